@@ -1,0 +1,169 @@
+/*
+ * sai.h -- C ABI of libsai, the GB300 (sm_103a) sparse-attention indexer
+ * decode path: FP8 paged MQA logits, then per-row top-k.
+ *
+ * Source of the operations.  The logits op and its arguments are those of
+ * `deepgemm_fp8_paged_mqa_logits(q_fp8, kv_cache, weights, out_logits,
+ * context_lens, block_tables, max_model_len, ...)` as called by the
+ * reproducer of aiter PR 4244 ("fix silent tail-row drop in
+ * deepgemm_fp8_paged_mqa_logits at large output stride", section "small
+ * reproducer"); the top-k is `top_k_per_row_decode`, which the same page's
+ * opening paragraph runs right after the logits launch to fill the
+ * persistent sparse-KV index buffer.  The scoring rule is the DeepSeek-style
+ * indexer definition
+ *
+ *     logits[r, t] = sum_h w[r, h] * ReLU(q[r, h] . k[t]) * scale[t]   (t < ctx_r)
+ *     logits[r, t] = -inf                                              (ctx_r <= t < W)
+ *
+ * with query row r = b * next_n + j and ctx_r = ctx_b - next_n + j + 1 (MTP
+ * row j sees one token more than row j - 1).
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" must be device memory (or managed memory) of
+ *     the current device.  Nothing is read from or written to host memory.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *     never synchronise.  They allocate nothing and keep no state across calls
+ *     apart from a per-process cache of the device's SM count.
+ *   - The caller owns every buffer.  The library keeps no pointer after the
+ *     call returns (kernels still in flight use them until they finish).
+ *   - Return value: SAI_OK (0), or a negative SAI_ERR_* code.  On any error
+ *     nothing is launched and no output is touched.
+ *   - Problems only the device can see (a page id outside the pool, a
+ *     context longer than the output or the block table, a pipeline wait that
+ *     ran out of time) never trap: they set bits in the optional device status
+ *     word (SAI_STATUS_*), which the library only ORs into and never clears.
+ *   - All byte offsets are formed in 64 bits: row bases are
+ *     int64(row) * stride, page bases int64(page_id) * page_bytes, so outputs
+ *     past 2^31 bytes and KV pages past 2^31 bytes are addressed correctly
+ *     (aiter PR 4244, section "Fix"; ATOM PR 2533, "[MLA] Address Triton
+ *     decode KV rows with int64 ids").
+ */
+#ifndef SAI_H_
+#define SAI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SAI_API __attribute__((visibility("default")))
+#else
+#define SAI_API
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* sai_stream_t;
+
+/* Return codes. */
+#define SAI_OK                    0
+#define SAI_ERR_INVALID_ARGUMENT (-1)  /* null pointer, negative size, stride < width, ... */
+#define SAI_ERR_UNSUPPORTED      (-2)  /* valid but not built: head_dim != 128, page size, ... */
+#define SAI_ERR_MISALIGNED       (-3)  /* a pointer lacks the alignment stated below */
+#define SAI_ERR_WORKSPACE        (-4)  /* top-k workspace missing or too small */
+#define SAI_ERR_CUDA             (-5)  /* a CUDA runtime call or kernel launch failed */
+
+/* Bits of the device status word (OR-ed in by kernels, never cleared). */
+#define SAI_STATUS_BAD_PAGE     0x1u  /* a block-table entry outside [0, num_pages): its tokens' logits are NaN */
+#define SAI_STATUS_CTX_CLAMPED  0x2u  /* a context_len < 0, > max_model_len or > table capacity: clamped */
+#define SAI_STATUS_TIMEOUT      0x4u  /* a bounded pipeline wait expired: the outputs of that CTA are incomplete */
+
+/* Paged K-cache byte layouts (kv_layout argument). */
+#define SAI_KV_PAGE_SPLIT   0  /* page = P*D value bytes (token-major), then P fp32 scales */
+#define SAI_KV_INTERLEAVED  1  /* page = P tokens of (D value bytes, then 4 scale bytes) */
+
+/*
+ * sai_paged_mqa_logits -- FP8 paged MQA logits (one launch).
+ *
+ *   q_fp8         device, uint8 [batch, next_n, heads, head_dim], contiguous,
+ *                 OCP e4m3fn bytes.  16-byte aligned.
+ *   kv_cache      device, uint8, num_pages pages of page_size * (head_dim + 4)
+ *                 bytes each, page p starting at byte p * page_size * (head_dim + 4)
+ *                 (the reproducer's [num_blocks, block_size, 1, head_dim + 4]
+ *                 byte tensor).  Inside a page, kv_layout decides where a
+ *                 token's head_dim e4m3fn values and its little-endian fp32
+ *                 scale lie (SAI_KV_PAGE_SPLIT: values of all page_size tokens
+ *                 first, token-major, then their page_size scales).
+ *                 16-byte aligned.  Only pages the block table names for
+ *                 t < ctx_r are read.
+ *   num_pages     pages in the pool (>= 1; page ids are checked against it).
+ *   page_size     tokens per page: 8, 16, 32, 64, 128 or 256.
+ *   weights       device, fp32 [batch * next_n, heads], contiguous.  16-byte aligned.
+ *   context_lens  device, int32 [batch]: tokens in each request's K-cache.
+ *   block_table   device, int32 [batch, block_table_stride]: page ids of each
+ *                 request, in token order (token t is in entry t / page_size).
+ *                 Entries past ceil(ctx_b / page_size) are never read.
+ *   block_table_stride  int32 entries between table rows (>= 1).
+ *   batch         requests (>= 0; 0 launches nothing).
+ *   next_n        query rows per request, 1..4 (MTP).
+ *   heads         64 or 128.
+ *   head_dim      must be 128.
+ *   logits        device, fp32 [batch * next_n, logits_stride]: receives
+ *                 columns [0, max_model_len) of every row; columns
+ *                 [max_model_len, logits_stride) are never written.  4-byte aligned.
+ *   logits_stride fp32 elements between rows (>= max_model_len); int64.
+ *   max_model_len W, the logical logits width (>= 1).
+ *   kv_layout     SAI_KV_PAGE_SPLIT or SAI_KV_INTERLEAVED.
+ *   status        nullable device uint32 word; SAI_STATUS_* bits are OR-ed in.
+ *   stream        stream to launch on.
+ *
+ * Every cell of [0, batch * next_n) x [0, W) is written on every call.  Row r
+ * sees ctx_r = clamp(ctx_b - next_n + j + 1, 0, min(W, block_table_stride *
+ * page_size)) tokens; the clamp raises SAI_STATUS_CTX_CLAMPED.
+ */
+SAI_API int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache,
+                         int64_t num_pages, int32_t page_size,
+                         const float* weights, const int32_t* context_lens,
+                         const int32_t* block_table, int64_t block_table_stride,
+                         int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim,
+                         float* logits, int64_t logits_stride, int64_t max_model_len,
+                         int32_t kv_layout, uint32_t* status, sai_stream_t stream);
+
+/*
+ * sai_top_k_workspace_bytes -- bytes of device workspace that
+ * sai_top_k_per_row_decode needs for `rows` rows of up to `max_len` columns and
+ * this k.  May be 0, in which case the workspace pointer may be null.
+ */
+SAI_API size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k);
+
+/*
+ * sai_top_k_per_row_decode -- per-row top-k of the logits (one launch).
+ *
+ *   logits        device, fp32 [batch * next_n, logits_stride] as written by
+ *                 sai_paged_mqa_logits.  4-byte aligned.
+ *   context_lens  device, int32 [batch]; row r = b * next_n + j considers
+ *                 columns [0, n_r) with n_r = clamp(ctx_b - next_n + j + 1, 0,
+ *                 max_model_len).
+ *   k             1 .. 65536.
+ *   indices       device, int32 [batch * next_n, indices_stride] (>= k): row r
+ *                 receives, in entries [0, k), the column indices of its
+ *                 min(k, n_r) largest logits, then -1 in every remaining entry
+ *                 up to k.  If n_r <= k the indices are exactly 0 .. n_r - 1.
+ *                 Entries are ordered by increasing column index among those
+ *                 strictly greater than the k-th largest value, followed by
+ *                 the ties at that value, lowest columns first.
+ *   workspace     device, workspace_bytes >= sai_top_k_workspace_bytes(...);
+ *                 may be null when that is 0.
+ *
+ * Every entry [0, k) of every row is written on every call (no stale indices
+ * survive in a persistent index buffer: aiter PR 4244, opening paragraph).
+ */
+SAI_API int sai_top_k_per_row_decode(const float* logits, int64_t logits_stride,
+                             const int32_t* context_lens, int32_t batch, int32_t next_n,
+                             int64_t max_model_len, int32_t k,
+                             int32_t* indices, int64_t indices_stride,
+                             void* workspace, size_t workspace_bytes, sai_stream_t stream);
+
+/* Static, human-readable name of a return code. */
+SAI_API const char* sai_error_string(int code);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+SAI_API int sai_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAI_H_ */

@@ -1,0 +1,195 @@
+"""Python binding of libsai, the GB300 sparse-attention indexer decode path.
+
+Thin ctypes marshalling over the C ABI declared in `include/sai.h`: each
+function checks tensor devices and dtypes, then passes raw device pointers,
+sizes and the current CUDA stream to the library.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If
+`libsai.so` has not been built, calls raise `LibraryNotBuilt`.
+
+    paged_mqa_logits(q, kv_cache, page_size, weights, context_lens, block_table,
+                     logits, max_model_len, ...)
+    top_k_per_row_decode(logits, context_lens, next_n, max_model_len, k, indices, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+__all__ = [
+    "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
+    "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
+    "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
+    "KV_PAGE_SPLIT", "KV_INTERLEAVED",
+]
+
+OK = 0
+ERR_INVALID_ARGUMENT = -1
+ERR_UNSUPPORTED = -2
+ERR_MISALIGNED = -3
+ERR_WORKSPACE = -4
+ERR_CUDA = -5
+
+STATUS_BAD_PAGE = 0x1
+STATUS_CTX_CLAMPED = 0x2
+STATUS_TIMEOUT = 0x4
+
+KV_PAGE_SPLIT = 0
+KV_INTERLEAVED = 1
+_LAYOUTS = {"split": KV_PAGE_SPLIT, "interleaved": KV_INTERLEAVED,
+            KV_PAGE_SPLIT: KV_PAGE_SPLIT, KV_INTERLEAVED: KV_INTERLEAVED}
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class SaiError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {error_string(code)} ({code})")
+
+
+_lib = None
+
+_c = ctypes
+_P = _c.c_void_p
+_SIGS = {
+    "sai_paged_mqa_logits": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int32, _P, _P, _P, _c.c_int64,
+                                        _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                        _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _P]),
+    "sai_top_k_workspace_bytes": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32]),
+    "sai_top_k_per_row_decode": (_c.c_int, [_P, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int64,
+                                            _c.c_int32, _P, _c.c_int64, _P, _c.c_size_t, _P]),
+    "sai_error_string": (_c.c_char_p, [_c.c_int]),
+    "sai_version": (_c.c_int, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libsai.so for sm_103a (in-tree) and load it."""
+    global _lib
+    path = _build.build(force=force, verbose=verbose)
+    _lib = None
+    library()
+    return path
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libsai (raises LibraryNotBuilt if it is missing)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise LibraryNotBuilt(f"{path} is missing: build it with "
+                                  "sparse_attention_indexer_03_gb300.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def error_string(code: int) -> str:
+    try:
+        return library().sai_error_string(code).decode()
+    except LibraryNotBuilt:
+        return f"code {code}"
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t, dtype, name):
+    import torch
+
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: dtype {t.dtype} not accepted")
+    return t.data_ptr()
+
+
+def paged_mqa_logits(q, kv_cache, page_size: int, weights, context_lens, block_table,
+                     logits, max_model_len: int, *, num_pages: Optional[int] = None,
+                     status=None, kv_layout="split", stream=None) -> None:
+    """FP8 paged MQA logits into `logits` (see `sai_paged_mqa_logits`).
+
+    q            uint8 or float8_e4m3fn [B, next_n, H, 128], contiguous
+    kv_cache     uint8 / float8 bytes of num_pages * page_size * 132 (any shape, contiguous)
+    weights      float32 [B * next_n, H], contiguous
+    context_lens int32 [B]
+    block_table  int32 [B, stride] (row stride from the tensor; inner stride 1)
+    logits       float32 [B * next_n, >= max_model_len] (row stride from the tensor)
+    status       optional int32/uint32-sized CUDA tensor of one element
+    """
+    import torch
+
+    u8 = (torch.uint8, torch.float8_e4m3fn)
+    if q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [B, next_n, H, D] tensor")
+    B, next_n, H, D = q.shape
+    if not kv_cache.is_contiguous() or not weights.is_contiguous():
+        raise ValueError("kv_cache and weights must be contiguous")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, stride] with unit inner stride")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [rows, stride] with unit inner stride")
+    page_bytes = page_size * (D + 4)
+    if num_pages is None:
+        num_pages = kv_cache.numel() * kv_cache.element_size() // page_bytes
+    code = library().sai_paged_mqa_logits(
+        _ptr(q, u8, "q"), _ptr(kv_cache, u8, "kv_cache"), int(num_pages), int(page_size),
+        _ptr(weights, torch.float32, "weights"), _ptr(context_lens, torch.int32, "context_lens"),
+        _ptr(block_table, torch.int32, "block_table"), int(block_table.stride(0)),
+        int(B), int(next_n), int(H), int(D),
+        _ptr(logits, torch.float32, "logits"), int(logits.stride(0)), int(max_model_len),
+        int(_LAYOUTS[kv_layout]), _ptr(status, (torch.int32, torch.uint32), "status"),
+        _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_paged_mqa_logits")
+
+
+def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:
+    return int(library().sai_top_k_workspace_bytes(int(rows), int(max_len), int(k)))
+
+
+def top_k_per_row_decode(logits, context_lens, next_n: int, max_model_len: int, k: int,
+                         indices, *, workspace=None, stream=None) -> None:
+    """Per-row top-k column indices into `indices` (see `sai_top_k_per_row_decode`).
+
+    logits   float32 [B * next_n, >= max_model_len] (row stride from the tensor)
+    indices  int32 [B * next_n, >= k] (row stride from the tensor)
+    """
+    import torch
+
+    if logits.stride(1) != 1 or indices.stride(1) != 1:
+        raise ValueError("logits and indices need unit inner stride")
+    B = context_lens.numel()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size()
+    code = library().sai_top_k_per_row_decode(
+        _ptr(logits, torch.float32, "logits"), int(logits.stride(0)),
+        _ptr(context_lens, torch.int32, "context_lens"), int(B), int(next_n), int(max_model_len), int(k),
+        _ptr(indices, torch.int32, "indices"), int(indices.stride(0)), ws_ptr, int(ws_bytes),
+        _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_top_k_per_row_decode")

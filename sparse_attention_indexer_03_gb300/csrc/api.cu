@@ -1,0 +1,113 @@
+// C ABI of libsai: argument validation and kernel launch.  Every check runs
+// before the first CUDA call, so a rejected call touches neither the device
+// nor any output.
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace sai {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool supported_page_size(int p) {
+  return p == 8 || p == 16 || p == 32 || p == 64 || p == 128 || p == 256;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAI_OK : SAI_ERR_CUDA; }
+
+}  // namespace
+}  // namespace sai
+
+extern "C" {
+
+int sai_version(void) { return 100; }
+
+const char* sai_error_string(int code) {
+  switch (code) {
+    case SAI_OK: return "ok";
+    case SAI_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case SAI_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case SAI_ERR_MISALIGNED: return "misaligned pointer";
+    case SAI_ERR_WORKSPACE: return "workspace missing or too small";
+    case SAI_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown error code";
+  }
+}
+
+int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                         const float* weights, const int32_t* context_lens, const int32_t* block_table,
+                         int64_t block_table_stride, int32_t batch, int32_t next_n, int32_t heads,
+                         int32_t head_dim, float* logits, int64_t logits_stride, int64_t max_model_len,
+                         int32_t kv_layout, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  if (batch < 0 || next_n < 1 || heads < 1 || head_dim < 1 || page_size < 1 || num_pages < 1 ||
+      block_table_stride < 1 || max_model_len < 1 || logits_stride < max_model_len)
+    return SAI_ERR_INVALID_ARGUMENT;
+  if (!q_fp8 || !kv_cache || !weights || !context_lens || !block_table || !logits) return SAI_ERR_INVALID_ARGUMENT;
+  if (kv_layout != SAI_KV_PAGE_SPLIT && kv_layout != SAI_KV_INTERLEAVED) return SAI_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim || !supported_page_size(page_size) || next_n > 4 || (heads != 64 && heads != 128))
+    return SAI_ERR_UNSUPPORTED;
+  // Byte extents must stay far inside int64.
+  if (num_pages > (INT64_MAX / 4) / ((int64_t)page_size * kTokenBytes)) return SAI_ERR_INVALID_ARGUMENT;
+  if (logits_stride > (INT64_MAX / 8) / ((int64_t)batch * next_n + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if (block_table_stride > (INT64_MAX / 8) / ((int64_t)batch + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if (batch > 65535) return SAI_ERR_UNSUPPORTED;
+  if (!aligned(q_fp8, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) || !aligned(context_lens, 4) ||
+      !aligned(block_table, 4) || !aligned(logits, 4) || !aligned(status, 4))
+    return SAI_ERR_MISALIGNED;
+  if (batch == 0) return SAI_OK;
+
+  LogitsArgs a;
+  a.q = q_fp8; a.kv = kv_cache; a.num_pages = num_pages; a.page_size = page_size;
+  a.weights = weights; a.context_lens = context_lens; a.block_table = block_table;
+  a.bt_stride = block_table_stride; a.batch = batch; a.next_n = next_n; a.heads = heads;
+  a.logits = logits; a.stride = logits_stride; a.width = max_model_len; a.layout = kv_layout;
+  a.status = status;
+  return from_cuda(launch_logits_simt(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k) {
+  if (rows < 0 || max_len < 0 || k < 1) return 0;
+  return sai::topk_workspace_bytes(rows, max_len, k);
+}
+
+int sai_top_k_per_row_decode(const float* logits, int64_t logits_stride, const int32_t* context_lens,
+                             int32_t batch, int32_t next_n, int64_t max_model_len, int32_t k,
+                             int32_t* indices, int64_t indices_stride, void* workspace, size_t workspace_bytes,
+                             sai_stream_t stream) {
+  using namespace sai;
+  if (batch < 0 || next_n < 1 || max_model_len < 1 || logits_stride < max_model_len || k < 1 ||
+      indices_stride < k)
+    return SAI_ERR_INVALID_ARGUMENT;
+  if (!logits || !context_lens || !indices) return SAI_ERR_INVALID_ARGUMENT;
+  if (k > 65536 || max_model_len > INT32_MAX) return SAI_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)batch * next_n;
+  if (rows > INT32_MAX) return SAI_ERR_UNSUPPORTED;
+  if (logits_stride > (INT64_MAX / 8) / (rows + 1) || indices_stride > (INT64_MAX / 8) / (rows + 1))
+    return SAI_ERR_INVALID_ARGUMENT;
+  if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(indices, 4)) return SAI_ERR_MISALIGNED;
+  const size_t need = topk_workspace_bytes((int)rows, max_model_len, k);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SAI_ERR_WORKSPACE;
+  if (rows == 0) return SAI_OK;
+
+  TopKArgs a;
+  a.logits = logits; a.stride = logits_stride; a.context_lens = context_lens; a.batch = batch;
+  a.next_n = next_n; a.width = max_model_len; a.k = k; a.indices = indices; a.out_stride = indices_stride;
+  return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

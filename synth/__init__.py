@@ -128,6 +128,17 @@ class Workload:
     def layout(self) -> str:
         return self.pool.layout
 
+    def to_device(self, device="cuda") -> dict:
+        """The inputs as device tensors: q, kv (flat pool bytes), weights,
+        context_lens, block_table."""
+        import torch
+
+        return dict(q=torch.from_numpy(self.q).to(device),
+                    kv=self.pool.to_device(device),
+                    weights=torch.from_numpy(self.weights).to(device),
+                    context_lens=torch.from_numpy(self.context_lens).to(device),
+                    block_table=torch.from_numpy(self.block_table).to(device))
+
 
 def _draw_pool(rng: np.random.Generator, num_pages: int, page_size: int,
                used_ids: np.ndarray, layout: str) -> KVPool:
