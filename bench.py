@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the indexer decode step: FP8 paged MQA logits, then per-row top-k.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|tiny|mtp|wide|kv2g|sweep:P,next_n,H,B,ctx]
+
+One step = one logits launch plus one top-k launch over one batch of synthetic
+inputs (the decode workload by default: B=64, next_n=1, H=64, D=128, P=64,
+ctx U[1024, 8192], W=8192, k=2048).  Metric: row-tokens per second,
+sum_r ctx_r / time, in Gtok/s, whole job over all ranks.
+
+Timing: inputs are resident in HBM; several input sets rotate so that the
+bytes one cycle touches exceed the 129 MB L2; the K steps run as replays of a
+CUDA graph of S steps, bracketed by a barrier and a device synchronise on
+both sides, timed with CUDA events; the slowest rank's time counts.  Events
+captured inside the graph give the per-launch durations of each kernel.
+
+Multi-GPU: one process per GPU (torchrun), each running its own batch of
+requests; no data-path collective (requests are independent), so scaling is
+weak.  `--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "indexer Gtokens/s (rows x context tokens) and % of FP8/HBM roofline, 1 GB300"
+UNIT = "Gtok/s"
+L2_BYTES = 129 * 2**20
+
+
+# ------------------------------------------------------------------ helpers
+def row_tokens(w) -> int:
+    """sum_r ctx_r: tokens each query row scores (row j of a request sees
+    ctx - next_n + j + 1 of them, clamped to [0, W])."""
+    ctx = w.context_lens.astype(np.int64)[:, None]
+    j = np.arange(w.next_n)[None, :]
+    cap = min(w.max_model_len, w.block_table.shape[1] * w.page_size)
+    return int(np.clip(ctx - w.next_n + j + 1, 0, cap).sum())
+
+
+def logits_bytes(w) -> int:
+    """Algorithmic HBM bytes of one logits launch: K values and scales once per
+    request, the block-table entries read, q and weights, context lengths, and
+    the full-width fp32 output."""
+    cap = min(w.max_model_len, w.block_table.shape[1] * w.page_size)
+    ctx = np.clip(w.context_lens.astype(np.int64), 0, cap)
+    kv = int(ctx.sum()) * (w.head_dim + 4)
+    table = int(np.ceil(ctx / w.page_size).sum()) * 4
+    qw = w.batch * w.next_n * w.heads * (w.head_dim + 4)
+    out = w.rows * w.max_model_len * 4
+    return kv + table + qw + out + 4 * w.batch
+
+
+def logits_flops(w) -> int:
+    return row_tokens(w) * 2 * w.heads * w.head_dim
+
+
+def topk_bytes(w) -> int:
+    return row_tokens(w) * 4 + w.rows * w.topk * 4
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def make_workload(name: str):
+    import synth
+
+    if name.startswith("sweep:"):
+        p, n, h, b, c = (int(x) for x in name.split(":", 1)[1].split(","))
+        return synth.sweep_point(p, n, h, b, c)
+    return synth.NAMED[name]()
+
+
+def describe(w) -> str:
+    return (f"{w.name}: B={w.batch}, next_n={w.next_n}, H={w.heads}, D={w.head_dim}, P={w.page_size}, "
+            f"W={w.max_model_len}, stride={w.logits_stride}, k={w.topk}, seed={w.seed}")
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per logits launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"logits_tc_{workload}.md")
+    src = os.path.join(ROOT, "sparse_attention_indexer_03_gb300", "csrc", "logits.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_sha(src):
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = [r.split(", ") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        under_load = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": float(np.median(under_load)) if under_load else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def aggregate(ms: float, tokens: int, world: int, device=None):
+    """Whole-job figures over the ranks: the slowest rank's time and the sum of
+    the row-tokens every rank processed per step.  Ranks hold independent
+    requests, so this is the only cross-rank exchange, and it lies outside the
+    timed region."""
+    if world <= 1:
+        return ms, tokens
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
+def rank_workload(name: str, rank: int):
+    """The batch of requests rank `rank` serves: the named workload (the same
+    shapes on every rank, weak scaling)."""
+    return make_workload(name)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step_sample(w, budget_s: float):
+    """Time the CPU oracle (logits, then top-k) over the workload's requests in
+    order until `budget_s` seconds have passed; returns (row_tokens, seconds, requests)."""
+    import oracle
+
+    ctx_rows = oracle.row_context_lengths(w.context_lens, w.next_n, w.max_model_len,
+                                          w.max_model_len, 1)
+    done_tok, reqs, t0 = 0, 0, time.perf_counter()
+    b = 0
+    while time.perf_counter() - t0 < budget_s:
+        rows = list(range(b * w.next_n, (b + 1) * w.next_n))
+        lg = oracle.paged_mqa_logits(w.q, w.pool.ids, w.pool.data, w.pool.num_pages, w.page_size,
+                                     w.weights, w.context_lens, w.block_table, w.next_n,
+                                     w.max_model_len, layout=w.layout, rows=rows)
+        oracle.top_k_per_row(lg.astype(np.float32), ctx_rows[rows], w.topk)
+        done_tok += int(ctx_rows[rows].sum())
+        reqs += 1
+        b = (b + 1) % w.batch
+    return done_tok, time.perf_counter() - t0, reqs
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload)
+    # Each step is a bounded sample: about 150 s of oracle work for the whole run.
+    budget = min(2.0, 150.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_step_sample(w, min(budget, 0.5))
+    tok, sec = 0, 0.0
+    reqs_total = 0
+    for _ in range(args.steps):
+        t, s, r = oracle_step_sample(w, budget)
+        tok += t
+        sec += s
+        reqs_total += r
+    value = tok / sec / 1e9
+    sample = (f"{reqs_total} requests of the {w.name} batch over {args.steps} steps "
+              f"(each step about {budget:.1f} s of oracle work: fp64 logits of the request's rows, then top-k)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(w)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_indexer_03_gb300 as sai
+
+    torch.cuda.set_device(local_rank)
+    sai.build()
+    dev = torch.device("cuda", local_rank)
+    w = rank_workload(args.workload, rank)
+    tok = row_tokens(w)
+
+    # Rotating input sets: enough that one cycle touches more bytes than L2.
+    touched = logits_bytes(w) + topk_bytes(w)
+    R = max(2, min(16, math.ceil(2.0 * L2_BYTES / max(touched, 1))))
+    sets = []
+    for _ in range(R):
+        d = w.to_device(dev)
+        d["logits"] = torch.empty((w.rows, w.logits_stride), dtype=torch.float32, device=dev)
+        d["indices"] = torch.empty((w.rows, w.topk), dtype=torch.int32, device=dev)
+        sets.append(d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(d):
+        sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
+                             d["block_table"], d["logits"], w.max_model_len, num_pages=w.pool.num_pages,
+                             status=status, stream=stream)
+        sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
+                                 d["indices"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(sets[i % R])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"status {int(status.item()):#x}"
+
+    # Graph of S steps with timing events around each kernel.
+    K = args.steps
+    S = K if K <= 200 else 100
+    K = S * math.ceil(K / S)
+    reps = K // S
+    try:
+        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(S)]
+    except TypeError:              # a torch without graph-recordable timing events
+        ev = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(S):
+            d = sets[i % R]
+            if ev:
+                ev[i][0].record(stream)
+            sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
+                                 d["block_table"], d["logits"], w.max_model_len, num_pages=w.pool.num_pages,
+                                 status=status, stream=stream)
+            if ev:
+                ev[i][1].record(stream)
+            sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
+                                     d["indices"], stream=stream)
+            if ev:
+                ev[i][2].record(stream)
+    graph.replay()                      # untimed: graph upload and warm-up
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    if ev:
+        logits_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(S)]
+        topk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(S)]
+    else:                          # per-kernel events on an eager pass over the same sets
+        logits_ms, topk_ms = [], []
+        with torch.cuda.stream(stream):
+            for i in range(S):
+                a, b2, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                d = sets[i % R]
+                a.record(stream)
+                sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
+                                     d["block_table"], d["logits"], w.max_model_len,
+                                     num_pages=w.pool.num_pages, status=status, stream=stream)
+                b2.record(stream)
+                sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
+                                         d["indices"], stream=stream)
+                c.record(stream)
+                torch.cuda.synchronize()
+                logits_ms.append(a.elapsed_time(b2))
+                topk_ms.append(b2.elapsed_time(c))
+    ms, tok_all = aggregate(ms, tok, world, dev)
+    assert int(status.item()) == 0, f"status {int(status.item()):#x}"
+
+    # End to end through the Python API: pinned host inputs in, indices out.
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in
+            (("q", w.q), ("weights", w.weights), ("context_lens", w.context_lens),
+             ("block_table", w.block_table))}
+    out_host = torch.empty((w.rows, w.topk), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    Ke = min(args.steps, 200)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(Ke + 3):
+            if i == 3:
+                e0.record(stream)
+            d = sets[i % R]
+            for k2, t in host.items():
+                d[k2].copy_(t, non_blocking=True)
+            step(d)
+            out_host.copy_(d["indices"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms, _ = aggregate(e2e_ms, tok, world, dev)
+
+    if rank != 0:
+        return 0
+    peaks = load_peaks()
+    lg_ms = float(np.mean(logits_ms))
+    tk_ms = float(np.mean(topk_ms))
+    lbytes = logits_bytes(w)
+    lflops = logits_flops(w)
+    fp8_peak_tflops = 2.0 * peaks["bf16_tflops"]          # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    t_hbm = lbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = lflops / (fp8_peak_tflops * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": lbytes / (lg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": lflops / (lg_ms * 1e-3) / 1e12, "peak": fp8_peak_tflops,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(w.name)
+    roof["kernel"] = "logits_tc_kernel"
+    roof["algorithmic_per_launch"] = lbytes if roof["bound"] == "hbm" else lflops
+    roof["peak_source"] = peaks["source"] + (" (fp8 = 2 x measured bf16)" if roof["bound"] == "tensor" else "")
+    value = tok_all * K / (ms * 1e-3) / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        ctok, csec, creqs = oracle_step_sample(w, float(os.environ.get("SAI_CPU_BASELINE_SECONDS", "12")))
+        cpu = {"value": ctok / csec / 1e9, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{creqs} requests of the {w.name} batch in order ({ctok} row-tokens), "
+                         f"fp64 logits then top-k, {csec:.1f} s"}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": describe(w), "row_tokens_per_step": tok,
+                       "l2": f"{R} rotating input sets, {R * touched / 2**20:.0f} MB touched per cycle > 129 MB L2",
+                       "timing": f"{K // S} replays of a CUDA graph of {S} steps",
+                       "logits_ms": lg_ms, "topk_ms": tk_ms,
+                       "topk_gbs": topk_bytes(w) / (tk_ms * 1e-3) / 1e9,
+                       "parallelism": f"replicas x{world} (independent requests per GPU)"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": tok_all * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"note: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -77,7 +77,11 @@ int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t 
   a.bt_stride = block_table_stride; a.batch = batch; a.next_n = next_n; a.heads = heads;
   a.logits = logits; a.stride = logits_stride; a.width = max_model_len; a.layout = kv_layout;
   a.status = status;
-  return from_cuda(launch_logits_simt(a, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Tensor cores for the page-split layout; its 132-byte token stride makes
+  // the interleaved layout unreachable for tiled TMA, so it runs on the CUDA cores.
+  if (kv_layout == SAI_KV_PAGE_SPLIT) return from_cuda(launch_logits_tc(a, st));
+  return from_cuda(launch_logits_simt(a, st));
 }
 
 size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k) {

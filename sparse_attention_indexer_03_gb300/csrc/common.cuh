@@ -57,6 +57,7 @@ struct LogitsArgs {
 };
 
 cudaError_t launch_logits_simt(const LogitsArgs& a, cudaStream_t stream);
+cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream);
 
 struct TopKArgs {
   const float* logits;

@@ -1,0 +1,578 @@
+// FP8 paged MQA logits on the sm_103a tensor cores.
+//
+//   logits[r, t] = sum_h w[r, h] * ReLU(q[b, j, h] . k[t]) * scale[t]   (t < ctx_r)
+//   logits[r, t] = -inf                                                 (ctx_r <= t < W)
+//
+// (the op `deepgemm_fp8_paged_mqa_logits` of aiter PR 4244, "small
+// reproducer"; rows r = b * next_n + j; MTP row j sees ctx_b - next_n + j + 1
+// tokens).
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0     work partition, then producer: block-table reads (int64
+//              widened, bounds-checked, one tile ahead) and TMA gathers of the
+//              K pages into a ring of 128-token stages.  A stage holds 128/P
+//              pages of P < 128 tokens, each its own TMA box, values and
+//              scales loaded separately (aiter PR 6626, "paged MQA logits:
+//              8-token pages ...", section 1), or half of a 256-token page.
+//              Q [next_n * H, 128] of each request is loaded once into one of
+//              two Q slots.
+//   warp 1     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
+//              A = the K stage (128 tokens x 128 B, K-major, 128-byte
+//              swizzle), B = Q (whole rows j, <= 256 columns per job), fp32
+//              accumulators in a ring of TMEM stages.
+//   warps 2-9  two epilogue warpgroups taking alternate jobs: tcgen05.ld of a
+//              token's accumulator row, ReLU, per-head weight, scale, -inf
+//              mask, coalesced stores at a 64-bit row base (aiter PR 4244,
+//              "Fix"); then their share of the -inf fill of columns past the
+//              last tile of each request.
+//
+// Work partition: the 128-token tiles of all requests, in request order,
+// split into equal contiguous ranges, one per CTA; the fill split the same
+// way in units of (row, 4096 columns).  Each CTA derives its range from
+// context_lens itself; there is no global scratch and no atomics.
+//
+// Every wait is bounded: when one runs out, the CTA raises SAI_STATUS_TIMEOUT,
+// stops, lets its in-flight copies and MMAs drain (again bounded), frees its
+// TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sai {
+namespace {
+
+constexpr int kTile = 128;                       // tokens per MMA tile (M)
+constexpr int kThreadsTc = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kStageBytes = kTile * kHeadDim;    // 16 KB of K values per stage
+constexpr int kScaleSlot = kTile * kScaleBytes;  // 512 B of scales per stage
+constexpr int kFillCols = 4096;
+constexpr long long kWaitBudget = 1LL << 31;     // SM clock cycles before a wait gives up
+constexpr int kMaxSmem = 232448;                 // dynamic shared memory per CTA on sm_100-family
+
+constexpr int kFlagNew = 1, kFlagLast = 2;
+
+struct TcParams {
+  const int32_t* context_lens;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const uint8_t* kv;
+  int64_t num_pages;
+  int page_size;
+  const float* weights;
+  float* logits;
+  int64_t stride;
+  int64_t width;
+  int64_t cap;          // min(W, bt_stride * P): longest context a row can have
+  int batch;
+  int stages;
+  uint32_t* status;
+};
+
+template <int NEXT_N, int H>
+struct Cfg {
+  static constexpr int N = NEXT_N * H;
+  static constexpr int NC = N <= 256 ? N : (N % 256 == 0 ? 256 : H);   // accumulator columns per job
+  static constexpr int C = N / NC;                                     // jobs per tile
+  static constexpr int ROWS = NC / H;                                  // rows j per job
+  static constexpr int ACC = NC <= 128 ? 4 : 2;                        // TMEM accumulator stages
+  static constexpr int TMEM_COLS = ACC * NC <= 256 ? 256 : 512;
+  static constexpr int QBOX = N <= 256 ? N : (N % 256 == 0 ? 256 : 192);
+  static constexpr int Q_BYTES = N * kHeadDim;
+  static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(kTile, NC);
+  static_assert(N % QBOX == 0 && NC % 16 == 0 && NC <= 256 && ACC * NC <= 512, "shape");
+};
+
+struct Part {        // this CTA's share of the work
+  int b0, t0, n_tiles;
+  int fb0, fu0, n_units;
+};
+
+struct SmemLayout {
+  uint32_t k, q, sc, meta, bar, misc, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc) {
+  SmemLayout L;
+  L.k = 0;
+  L.q = L.k + stages * kStageBytes;
+  L.sc = L.q + 2 * q_bytes;
+  L.meta = L.sc + stages * kScaleSlot;
+  L.bar = L.meta + stages * 16;
+  L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1);
+  L.total = L.misc + 64;
+  return L;
+}
+
+__device__ __forceinline__ int64_t ctx_eff(int64_t raw, int64_t cap) { return raw < 0 ? 0 : (raw > cap ? cap : raw); }
+
+__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int64_t warp_incl_scan64(int64_t v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// Tiles of request b (compute part) and its fill units.
+__device__ __forceinline__ int64_t req_tiles(int64_t ce) { return (ce + kTile - 1) / kTile; }
+template <int NEXT_N>
+__device__ __forceinline__ int64_t req_units(int64_t ce, int64_t W) {
+  const int64_t fs = min(W, req_tiles(ce) * kTile);
+  return (int64_t)NEXT_N * ((W - fs + kFillCols - 1) / kFillCols);
+}
+
+// Warp 0: split the tiles and the fill units of all requests evenly across
+// the grid and locate this CTA's first tile and first unit.
+template <int NEXT_N>
+__device__ void compute_partition(const TcParams& p, Part* part, int lane) {
+  int64_t T = 0, U = 0;
+  bool clamped = false;
+  for (int b = lane; b < p.batch; b += 32) {
+    const int64_t raw = p.context_lens[b];
+    clamped |= raw < 0 || raw > p.cap;
+    const int64_t ce = ctx_eff(raw, p.cap);
+    T += req_tiles(ce);
+    U += req_units<NEXT_N>(ce, p.width);
+  }
+  T = warp_sum64(T);
+  U = warp_sum64(U);
+  if (blockIdx.x == 0 && __any_sync(0xffffffffu, clamped) && lane == 0) raise_status(p.status, SAI_STATUS_CTX_CLAMPED);
+  const int64_t G = gridDim.x, i = blockIdx.x;
+  const int64_t tb = T * i / G, te = T * (i + 1) / G;
+  const int64_t ub = U * i / G, ue = U * (i + 1) / G;
+  int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
+  int64_t ct = 0, cu = 0;
+  bool got_t = tb >= te, got_u = ub >= ue;
+  for (int base = 0; base < p.batch && !(got_t && got_u); base += 32) {
+    const int b = base + lane;
+    const int64_t ce = b < p.batch ? ctx_eff(p.context_lens[b], p.cap) : 0;
+    const int64_t x = b < p.batch ? req_tiles(ce) : 0;
+    const int64_t y = b < p.batch ? req_units<NEXT_N>(ce, p.width) : 0;
+    const int64_t xi = warp_incl_scan64(x, lane), yi = warp_incl_scan64(y, lane);
+    const bool ht = !got_t && x > 0 && ct + xi - x <= tb && tb < ct + xi;
+    const bool hu = !got_u && y > 0 && cu + yi - y <= ub && ub < cu + yi;
+    const uint32_t bt = __ballot_sync(0xffffffffu, ht), bu = __ballot_sync(0xffffffffu, hu);
+    if (bt) {
+      const int src = __ffs(bt) - 1;
+      b0 = __shfl_sync(0xffffffffu, b, src);
+      t0 = (int)__shfl_sync(0xffffffffu, tb - (ct + xi - x), src);
+      got_t = true;
+    }
+    if (bu) {
+      const int src = __ffs(bu) - 1;
+      fb0 = __shfl_sync(0xffffffffu, b, src);
+      fu0 = (int)__shfl_sync(0xffffffffu, ub - (cu + yi - y), src);
+      got_u = true;
+    }
+    ct += __shfl_sync(0xffffffffu, xi, 31);
+    cu += __shfl_sync(0xffffffffu, yi, 31);
+  }
+  if (lane == 0) {
+    part->b0 = b0; part->t0 = t0; part->n_tiles = (int)(te - tb);
+    part->fb0 = fb0; part->fu0 = fu0; part->n_units = (int)(ue - ub);
+  }
+}
+
+// Context lengths of requests [base, base + 32) held one per lane, so a warp
+// walking requests in order reads them from registers.
+struct CtxCache {
+  int base = -1000000;
+  int64_t mine = 0;
+  __device__ __forceinline__ int64_t get(const TcParams& p, int b, int lane) {
+    if (b < base || b >= base + 32) {              // warp-uniform
+      base = b;
+      mine = (b + lane < p.batch) ? (int64_t)p.context_lens[b + lane] : 0;
+    }
+    return __shfl_sync(0xffffffffu, mine, b - base);
+  }
+};
+
+template <int NEXT_N, int H>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
+                 const TcParams p) {
+  using K = Cfg<NEXT_N, H>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stages = p.stages;
+  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC);
+  const uint32_t s_base = ptx::smem_addr(smem);
+  const uint32_t s_k = s_base + L.k, s_q = s_base + L.q;
+  float* scales = reinterpret_cast<float*>(smem + L.sc);
+  int4* meta = reinterpret_cast<int4*>(smem + L.meta);
+  const uint32_t bar = s_base + L.bar;
+  // barrier addresses
+  auto full = [&](int s) { return bar + 8u * s; };
+  auto kempty = [&](int s) { return bar + 8u * (stages + s); };
+  auto qfull = [&](int q) { return bar + 8u * (2 * stages + q); };
+  auto qempty = [&](int q) { return bar + 8u * (2 * stages + 2 + q); };
+  auto tfull = [&](int a) { return bar + 8u * (2 * stages + 4 + a); };
+  auto tempty = [&](int a) { return bar + 8u * (2 * stages + 4 + K::ACC + a); };
+  const uint32_t drain = bar + 8u * (2 * stages + 4 + 2 * K::ACC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  Part* part = reinterpret_cast<Part*>(smem + L.misc + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- set-up --------------------------------------------------------------
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmap_kv);
+      ptx::prefetch_tensormap(&tmap_q);
+    }
+    compute_partition<NEXT_N>(p, part, lane);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int s = 0; s < stages; ++s) {
+        ptx::mbar_init(full(s), 1);
+        ptx::mbar_init(kempty(s), 1 + 4 * K::C);
+      }
+      for (int q = 0; q < 2; ++q) {
+        ptx::mbar_init(qfull(q), 1);
+        ptx::mbar_init(qempty(q), 1);
+      }
+      for (int a = 0; a < K::ACC; ++a) {
+        ptx::mbar_init(tfull(a), 1);
+        ptx::mbar_init(tempty(a), 4);
+      }
+      ptx::mbar_init(drain, 1);
+      *abort_flag = 0;
+      ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    ptx::tmem_alloc(ptx::smem_addr(tmem_holder), K::TMEM_COLS);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Part pt = *part;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_status(p.status, SAI_STATUS_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ---- producer ------------------------------------------------------------
+    const uint64_t pol_k = ptx::policy_evict_first();
+    const uint64_t pol_q = ptx::policy_evict_last();
+    const int P = p.page_size;
+    const int ppt = P >= kTile ? 1 : kTile / P;          // pages per tile
+    const int tok_per_box = P >= kTile ? kTile : P;
+    const uint32_t box_bytes = (uint32_t)tok_per_box * kTokenBytes;
+    CtxCache cc;
+    int b = pt.b0, t = pt.t0;
+    int64_t raw = pt.n_tiles > 0 ? cc.get(p, b, lane) : 0;
+    int64_t ce = ctx_eff(raw, p.cap), nt = req_tiles(ce);
+    int q_count = 0;
+    // page ids of the current tile (one lane per page)
+    auto page_of = [&](int bb, int tt, int64_t cee) -> int64_t {
+      const int64_t tok0 = (int64_t)tt * kTile + (P >= kTile ? 0 : (int64_t)lane * P);
+      if (lane >= ppt || tok0 >= cee) return -2;                          // not needed
+      return (int64_t)p.block_table[(int64_t)bb * p.bt_stride + tok0 / P];   // widened before use
+    };
+    int64_t pg = pt.n_tiles > 0 ? page_of(b, t, ce) : -2;
+    bool ok = true;
+    int i = 0;
+    for (; i < pt.n_tiles && ok; ++i) {
+      const int s = i % stages;
+      const uint32_t ph = (uint32_t)(i / stages) & 1u;
+      const bool is_new = (i == 0) || (t == 0);
+      const bool is_last = (t == nt - 1) || (i == pt.n_tiles - 1);
+      // next tile's coordinates and page ids, loaded ahead of the waits
+      int bn = b, tn = t + 1;
+      int64_t rawn = raw, cen = ce, ntn = nt;
+      if (tn == nt && i + 1 < pt.n_tiles) {
+        do {
+          ++bn;
+          rawn = cc.get(p, bn, lane);
+          cen = ctx_eff(rawn, p.cap);
+          ntn = req_tiles(cen);
+        } while (ntn == 0 && bn + 1 < p.batch);
+        tn = 0;
+      }
+      const int64_t pg_next = (i + 1 < pt.n_tiles) ? page_of(bn, tn, cen) : -2;
+
+      if (is_new) {
+        const int qs = q_count & 1;
+        if (!ptx::mbar_wait_warp(qempty(qs), ((uint32_t)(q_count >> 1) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(qfull(qs), K::Q_BYTES);
+          for (int x = 0; x < K::N / K::QBOX; ++x)
+            ptx::tma_load_2d(s_q + qs * K::Q_BYTES + x * K::QBOX * kHeadDim, &tmap_q, 0, b * K::N + x * K::QBOX,
+                             qfull(qs), pol_q);
+        }
+        ++q_count;
+      }
+      if (!ptx::mbar_wait_warp(kempty(s), ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
+      const bool need = pg != -2;
+      const bool bad = need && (pg < 0 || pg >= p.num_pages);
+      const bool load = need && !bad;
+      const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
+      if (bad) {
+        for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : lane * P) + x] = __int_as_float(0x7fc00000);
+        ptx::fence_proxy_async_smem();
+        raise_status(p.status, SAI_STATUS_BAD_PAGE);
+      }
+      if (lane == 0) {
+        meta[s] = make_int4(b, t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, raw)),
+                            (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (((q_count - 1) & 1) << 8));
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes);
+      __syncwarp();
+      if (load) {
+        const int y = P > kTile ? (t & 1) * kTile : 0;                           // half of a 256-token page
+        const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : lane * P * kHeadDim);
+        ptx::tma_load_3d(dst, &tmap_kv, 0, y, (int)pg, full(s), pol_k);
+        const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)P * kHeadDim + (int64_t)y * kScaleBytes;
+        const uint32_t sdst = s_base + L.sc + s * kScaleSlot + (P >= kTile ? 0 : lane * P * kScaleBytes);
+        ptx::bulk_load(sdst, src, (uint32_t)tok_per_box * kScaleBytes, full(s), pol_k);
+      }
+      b = bn; t = tn; raw = rawn; ce = cen; nt = ntn; pg = pg_next;
+    }
+    if (!ok) {
+      // Let the copies already issued land before the CTA exits.
+      const int zero_flag = 0;
+      for (int k2 = max(0, i - stages); k2 < i; ++k2)
+        ptx::mbar_wait_warp(full(k2 % stages), (uint32_t)(k2 / stages) & 1u, &zero_flag, 1LL << 26);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer -------------------------------------------------------------
+    if (lane == 0) {
+      int q_count = 0, acc_count = 0;
+      bool aborted = false;
+      for (int i = 0; i < pt.n_tiles; ++i) {
+        const int s = i % stages;
+        if (!ptx::mbar_wait(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
+        ptx::tc_fence_after();
+        const int4 m = meta[s];
+        const int qs = (m.w >> 8) & 1;
+        if (m.w & kFlagNew) {
+          if (!ptx::mbar_wait(qfull(qs), (uint32_t)(q_count >> 1) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
+          ++q_count;
+          ptx::tc_fence_after();
+        }
+        bool ok = true;
+#pragma unroll 1
+        for (int c = 0; c < K::C; ++c, ++acc_count) {
+          const int a = acc_count % K::ACC;
+          if (!ptx::mbar_wait(tempty(a), ((uint32_t)(acc_count / K::ACC) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem_base + (uint32_t)(a * K::NC);
+          const uint64_t adesc = ptx::desc_kmajor_sw128(s_k + s * kStageBytes);
+          const uint64_t bdesc = ptx::desc_kmajor_sw128(s_q + qs * K::Q_BYTES + c * K::NC * kHeadDim);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 32; ++k)       // 32 bytes of K per instruction: +2 in 16-byte units
+            ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, K::IDESC, k > 0 ? 1u : 0u);
+          ptx::mma_commit(tfull(a));
+        }
+        if (!ok) { fail(); aborted = true; break; }
+        ptx::mma_commit(kempty(s));
+        if (m.w & kFlagLast) ptx::mma_commit(qempty(qs));
+      }
+      // After an abort, the MMAs already issued complete before TMEM is freed
+      // (otherwise the epilogue has already seen every one of them complete).
+      if (aborted) {
+        const int zero_flag = 0;
+        ptx::mma_commit(drain);
+        ptx::mbar_wait(drain, 0, &zero_flag, 1LL << 28);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue ---------------------------------------------------------------
+    const int ew = warp - 2;
+    const int wg = ew >> 2;
+    const int quarter = warp & 3;                 // TMEM lanes this warp may read
+    const int token = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const int jobs = pt.n_tiles * K::C;
+    for (int a = wg; a < jobs; a += 2) {
+      const int i = a / K::C, c = a % K::C, s = i % stages;
+      const int acc = a % K::ACC;
+      if (!ptx::mbar_wait_warp(tfull(acc), (uint32_t)(a / K::ACC) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
+      if (!ptx::mbar_wait_warp(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
+      const int4 m = meta[s];
+      const float sc = scales[s * kTile + token];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(kempty(s));
+      ptx::tc_fence_after();
+      float out[K::ROWS];
+#pragma unroll
+      for (int jr = 0; jr < K::ROWS; ++jr) {
+        const int j = c * K::ROWS + jr;
+        const float4* wrow = reinterpret_cast<const float4*>(p.weights + ((int64_t)m.x * NEXT_N + j) * H);
+        float accum = 0.f;
+#pragma unroll
+        for (int h0 = 0; h0 < H; h0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32(t_lane + (uint32_t)(acc * K::NC + jr * H + h0), v);
+          float4 w4[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) w4[x] = __ldg(wrow + (h0 >> 2) + x);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            accum = fmaf(w4[x].x, fmaxf(__uint_as_float(v[4 * x + 0]), 0.f), accum);
+            accum = fmaf(w4[x].y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), accum);
+            accum = fmaf(w4[x].z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), accum);
+            accum = fmaf(w4[x].w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), accum);
+          }
+        }
+        out[jr] = accum;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty(acc));
+      const int64_t col = (int64_t)m.y * kTile + token;
+      if (col < p.width) {
+#pragma unroll
+        for (int jr = 0; jr < K::ROWS; ++jr) {
+          const int j = c * K::ROWS + jr;
+          const int64_t n_r = row_context(m.z, NEXT_N, j, p.cap);
+          const int64_t r = (int64_t)m.x * NEXT_N + j;
+          p.logits[r * p.stride + col] = col < n_r ? out[jr] * sc : -INFINITY;   // 64-bit row base
+        }
+      }
+    }
+    // ---- -inf fill past each request's last tile ------------------------------
+    CtxCache cc;
+    int b = pt.fb0;
+    int64_t u_in = pt.fu0;
+    int64_t ce = pt.n_units > 0 ? ctx_eff(cc.get(p, b, lane), p.cap) : 0;
+    int64_t fs = min(p.width, req_tiles(ce) * kTile);
+    int64_t chunks = (p.width - fs + kFillCols - 1) / kFillCols;
+    for (int u = 0; u < pt.n_units; ++u) {
+      while (u_in >= NEXT_N * chunks && b < p.batch) {   // move to the next request with fill
+        ++b;
+        u_in = 0;
+        ce = ctx_eff(cc.get(p, b, lane), p.cap);
+        fs = min(p.width, req_tiles(ce) * kTile);
+        chunks = (p.width - fs + kFillCols - 1) / kFillCols;
+      }
+      if (b >= p.batch) break;                          // never past the last row
+      if (u % kEpiWarps == ew) {
+        const int j = (int)(u_in / chunks);
+        const int64_t c0 = fs + (u_in % chunks) * kFillCols;
+        const int64_t c1 = min(p.width, c0 + kFillCols);
+        float* row = p.logits + ((int64_t)b * NEXT_N + j) * p.stride;    // 64-bit row base
+        int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(row + c0) & 15)) & 15) >> 2);
+        head = min(head, c1 - c0);
+        if (lane < head) row[c0 + lane] = -INFINITY;
+        const int64_t v0 = c0 + head;
+        const int64_t nv = (c1 - v0) >> 2;
+        float4* vrow = reinterpret_cast<float4*>(row + v0);
+        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int64_t x = lane; x < nv; x += 32) vrow[x] = ninf;
+        const int64_t tail0 = v0 + nv * 4;
+        if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
+      }
+      ++u_in;
+    }
+  }
+
+  // ---- tear-down ----------------------------------------------------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, K::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+template <int NEXT_N, int H>
+cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
+  using K = Cfg<NEXT_N, H>;
+  EncodeTiled enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const int P = a.page_size;
+  CUtensorMap tkv, tq;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)P,
+                                (cuuint64_t)(a.num_pages < (int64_t)INT32_MAX ? a.num_pages : (int64_t)INT32_MAX)};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)P * kTokenBytes};
+    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)min(P, kTile), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.batch * K::N};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)K::QBOX};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int per_stage = kStageBytes + kScaleSlot + 16 + 16;
+  const int fixed = 1024 + 2 * K::Q_BYTES + 8 * (4 + 2 * K::ACC + 1) + 64;
+  const int stages = min(8, (kMaxSmem - fixed) / per_stage);
+  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC);
+  const size_t smem = (size_t)L.total + 1024;
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H>, smem, smem_set);
+  if (e != cudaSuccess) return e;
+
+  TcParams p;
+  p.context_lens = a.context_lens; p.block_table = a.block_table; p.bt_stride = a.bt_stride;
+  p.kv = a.kv; p.num_pages = a.num_pages; p.page_size = P; p.weights = a.weights;
+  p.logits = a.logits; p.stride = a.stride; p.width = a.width;
+  p.cap = min(a.width, a.bt_stride * (int64_t)P);
+  p.batch = a.batch; p.stages = stages; p.status = a.status;
+  const int grid = device_sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  logits_tc_kernel<NEXT_N, H><<<grid, kThreadsTc, smem, stream>>>(tkv, tq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream) {
+  switch (a.next_n * 1000 + a.heads) {
+    case 1064: return launch_tc<1, 64>(a, stream);
+    case 2064: return launch_tc<2, 64>(a, stream);
+    case 3064: return launch_tc<3, 64>(a, stream);
+    case 4064: return launch_tc<4, 64>(a, stream);
+    case 1128: return launch_tc<1, 128>(a, stream);
+    case 2128: return launch_tc<2, 128>(a, stream);
+    case 3128: return launch_tc<3, 128>(a, stream);
+    case 4128: return launch_tc<4, 128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sai
