@@ -305,7 +305,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                      d["indices"], stream=stream)
             if ev:
                 ev[i][2].record(stream)
-    graph.replay()                      # untimed: graph upload and warm-up
+    with torch.cuda.stream(stream):
+        graph.replay()                  # untimed: graph upload and warm-up
     torch.cuda.synchronize()
 
     if world > 1:
@@ -314,10 +315,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
-        t_start.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        t_end.record(stream)
+        with torch.cuda.stream(stream):          # replay() launches on the current stream
+            t_start.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()

@@ -8,19 +8,23 @@
 // tokens).
 //
 // One persistent CTA per SM, warp-specialised:
-//   warp 0     work partition, then producer: block-table reads (int64
-//              widened, bounds-checked, one tile ahead) and TMA gathers of the
-//              K pages into a ring of 128-token stages.  A stage holds 128/P
-//              pages of P < 128 tokens, each its own TMA box, values and
-//              scales loaded separately (aiter PR 6626, "paged MQA logits:
-//              8-token pages ...", section 1), or half of a 256-token page.
-//              Q [next_n * H, 128] of each request is loaded once into one of
+//   warps 0-2  producers, taking the tiles round-robin: block-table reads
+//              (int64 widened, bounds-checked, copied ahead with cp.async) and
+//              TMA gathers of the K pages into a ring of 128-token stages.  A
+//              stage holds 128/P pages of P < 128 tokens, each its own pair of
+//              TMA boxes, values and scales loaded separately (aiter PR 6626,
+//              "paged MQA logits: 8-token pages ...", section 1), or half of a
+//              256-token page.  A copy instruction costs the issuing warp
+//              hundreds of cycles whatever its size, so a tile's page copies
+//              go out as one warp-wide instruction (one lane per page) and
+//              three warps issue in parallel.  Warp 0 also computes the work partition.  Q
+//              [next_n * H, 128] of each request is loaded once into one of
 //              two Q slots.
-//   warp 1     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
+//   warp 3     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
 //              A = the K stage (128 tokens x 128 B, K-major, 128-byte
 //              swizzle), B = Q (whole rows j, <= 256 columns per job), fp32
 //              accumulators in a ring of TMEM stages.
-//   warps 2-9  two epilogue warpgroups taking alternate jobs: tcgen05.ld of a
+//   warps 4-11 two epilogue warpgroups taking alternate jobs: tcgen05.ld of a
 //              token's accumulator row, ReLU, per-head weight, scale, -inf
 //              mask, coalesced stores at a 64-bit row base (aiter PR 4244,
 //              "Fix"); then their share of the -inf fill of columns past the
@@ -43,15 +47,19 @@ namespace sai {
 namespace {
 
 constexpr int kTile = 128;                       // tokens per MMA tile (M)
-constexpr int kThreadsTc = 320;
+constexpr int kProducers = 3;                    // producer warps 0 .. kProducers - 1
+constexpr int kMmaWarp = kProducers;             // then the MMA warp
+constexpr int kFirstEpiWarp = kProducers + 1;    // then two epilogue warpgroups
 constexpr int kEpiWarps = 8;
+constexpr int kThreadsTc = (kProducers + 1 + kEpiWarps) * 32;
 constexpr int kStageBytes = kTile * kHeadDim;    // 16 KB of K values per stage
-constexpr int kScaleSlot = kTile * kScaleBytes;  // 512 B of scales per stage
+constexpr int kScaleSlot = kTile * kScaleBytes;  // 512 B of scales per stage, in token order
 constexpr int kFillCols = 4096;
 constexpr long long kWaitBudget = 1LL << 31;     // SM clock cycles before a wait gives up
 constexpr int kMaxSmem = 232448;                 // dynamic shared memory per CTA on sm_100-family
 
 constexpr int kFlagNew = 1, kFlagLast = 2;
+constexpr int kLookahead = 8;                    // tiles of page ids copied ahead of the producer
 
 struct TcParams {
   const int32_t* context_lens;
@@ -66,7 +74,6 @@ struct TcParams {
   int64_t width;
   int64_t cap;          // min(W, bt_stride * P): longest context a row can have
   int batch;
-  int stages;
   uint32_t* status;
 };
 
@@ -81,6 +88,11 @@ struct Cfg {
   static constexpr int QBOX = N <= 256 ? N : (N % 256 == 0 ? 256 : 192);
   static constexpr int Q_BYTES = N * kHeadDim;
   static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(kTile, NC);
+  // K ring depth: as many 128-token stages as fit beside two Q slots (at most 8).
+  static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64;
+  static constexpr int PER_STAGE = kStageBytes + kScaleSlot + 16 + 16;
+  static constexpr int STAGES = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
+  static_assert(STAGES >= 2, "shared memory");
   static_assert(N % QBOX == 0 && NC % 16 == 0 && NC <= 256 && ACC * NC <= 512, "shape");
 };
 
@@ -90,7 +102,7 @@ struct Part {        // this CTA's share of the work
 };
 
 struct SmemLayout {
-  uint32_t k, q, sc, meta, bar, misc, total;
+  uint32_t k, q, sc, meta, ids, bar, misc, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc) {
@@ -99,7 +111,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int a
   L.q = L.k + stages * kStageBytes;
   L.sc = L.q + 2 * q_bytes;
   L.meta = L.sc + stages * kScaleSlot;
-  L.bar = L.meta + stages * 16;
+  L.ids = L.meta + stages * 16;
+  L.bar = L.ids + kProducers * kLookahead * 32 * 4;
   L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1);
   L.total = L.misc + 64;
   return L;
@@ -131,17 +144,39 @@ __device__ __forceinline__ int64_t req_units(int64_t ce, int64_t W) {
 }
 
 // Warp 0: split the tiles and the fill units of all requests evenly across
-// the grid and locate this CTA's first tile and first unit.
+// the grid and locate this CTA's first tile and first unit.  Up to
+// 32 * kCtxRegs context lengths are read once into registers (one round of
+// loads in flight); longer batches are read in two passes.
+constexpr int kCtxRegs = 16;
+
 template <int NEXT_N>
 __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
+  const bool in_regs = p.batch <= 32 * kCtxRegs;
+  int64_t ce_r[kCtxRegs];
   int64_t T = 0, U = 0;
   bool clamped = false;
-  for (int b = lane; b < p.batch; b += 32) {
-    const int64_t raw = p.context_lens[b];
-    clamped |= raw < 0 || raw > p.cap;
-    const int64_t ce = ctx_eff(raw, p.cap);
-    T += req_tiles(ce);
-    U += req_units<NEXT_N>(ce, p.width);
+  if (in_regs) {
+    int32_t raw_r[kCtxRegs];
+#pragma unroll
+    for (int x = 0; x < kCtxRegs; ++x) {
+      const int b = x * 32 + lane;
+      raw_r[x] = b < p.batch ? p.context_lens[b] : 0;
+    }
+#pragma unroll
+    for (int x = 0; x < kCtxRegs; ++x) {
+      clamped |= raw_r[x] < 0 || raw_r[x] > p.cap;
+      ce_r[x] = ctx_eff(raw_r[x], p.cap);
+      T += req_tiles(ce_r[x]);
+      U += req_units<NEXT_N>(ce_r[x], p.width);
+    }
+  } else {
+    for (int b = lane; b < p.batch; b += 32) {
+      const int64_t raw = p.context_lens[b];
+      clamped |= raw < 0 || raw > p.cap;
+      const int64_t ce = ctx_eff(raw, p.cap);
+      T += req_tiles(ce);
+      U += req_units<NEXT_N>(ce, p.width);
+    }
   }
   T = warp_sum64(T);
   U = warp_sum64(U);
@@ -152,9 +187,7 @@ __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
   int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
   int64_t ct = 0, cu = 0;
   bool got_t = tb >= te, got_u = ub >= ue;
-  for (int base = 0; base < p.batch && !(got_t && got_u); base += 32) {
-    const int b = base + lane;
-    const int64_t ce = b < p.batch ? ctx_eff(p.context_lens[b], p.cap) : 0;
+  auto step = [&](int b, int64_t ce) {
     const int64_t x = b < p.batch ? req_tiles(ce) : 0;
     const int64_t y = b < p.batch ? req_units<NEXT_N>(ce, p.width) : 0;
     const int64_t xi = warp_incl_scan64(x, lane), yi = warp_incl_scan64(y, lane);
@@ -175,6 +208,16 @@ __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
     }
     ct += __shfl_sync(0xffffffffu, xi, 31);
     cu += __shfl_sync(0xffffffffu, yi, 31);
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int x = 0; x < kCtxRegs; ++x)
+      if (x * 32 < p.batch && !(got_t && got_u)) step(x * 32 + lane, ce_r[x]);
+  } else {
+    for (int base = 0; base < p.batch && !(got_t && got_u); base += 32) {
+      const int b = base + lane;
+      step(b, b < p.batch ? ctx_eff(p.context_lens[b], p.cap) : 0);
+    }
   }
   if (lane == 0) {
     part->b0 = b0; part->t0 = t0; part->n_tiles = (int)(te - tb);
@@ -196,6 +239,34 @@ struct CtxCache {
   }
 };
 
+// Position (request b, tile t) in the walk over a CTA's tiles, with the
+// request's raw and clamped context and its tile count.
+struct Cursor {
+  int b = 0, t = 0;
+  int64_t raw = 0, ce = 0, nt = 0;
+  __device__ __forceinline__ void load(const TcParams& p, CtxCache& cc, int lane) {
+    raw = cc.get(p, b, lane);
+    ce = ctx_eff(raw, p.cap);
+    nt = req_tiles(ce);
+  }
+  __device__ __forceinline__ void start(const TcParams& p, int b0, int t0, CtxCache& cc, int lane) {
+    b = b0;
+    t = t0;
+    load(p, cc, lane);
+  }
+  // Next tile; skips requests without tiles (the partition guarantees one
+  // follows).  Returns 1 when the tile belongs to a new request.
+  __device__ __forceinline__ int advance(const TcParams& p, CtxCache& cc, int lane) {
+    if (++t < nt) return 0;
+    t = 0;
+    do {
+      ++b;
+      load(p, cc, lane);
+    } while (nt == 0 && b + 1 < p.batch);
+    return 1;
+  }
+};
+
 template <int NEXT_N, int H>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
@@ -203,7 +274,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   using K = Cfg<NEXT_N, H>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stages = p.stages;
+  constexpr int stages = K::STAGES;
   const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC);
   const uint32_t s_base = ptx::smem_addr(smem);
   const uint32_t s_k = s_base + L.k, s_q = s_base + L.q;
@@ -230,8 +301,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       ptx::prefetch_tensormap(&tmap_kv);
       ptx::prefetch_tensormap(&tmap_q);
     }
+    // Inputs may come from the previous kernel in the stream, and the logits
+    // buffer may still be read by it: wait for it before touching either.
+    ptx::wait_prerequisites();
     compute_partition<NEXT_N>(p, part, lane);
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
         ptx::mbar_init(full(s), 1);
@@ -252,103 +326,147 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     __syncwarp();
     ptx::tmem_alloc(ptx::smem_addr(tmem_holder), K::TMEM_COLS);
   }
+  ptx::wait_prerequisites();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const Part pt = *part;
+  // The next kernel in the stream (top-k) may be scheduled now; it still
+  // waits for this grid to complete before it reads the logits.
+  ptx::launch_dependents();
 
   auto fail = [&]() {
     *abort_flag = 1;
     raise_status(p.status, SAI_STATUS_TIMEOUT);
   };
 
-  if (warp == 0) {
-    // ---- producer ------------------------------------------------------------
+  if (warp < kProducers) {
+    // ---- producers: warp pw issues tiles pw, pw + kProducers, ... ----------------
+    // A tile's copies go out as two warp instructions: lane l loads the values
+    // of page l of the tile (a 128-byte swizzled tensor box), then its scales
+    // (a contiguous bulk copy).
+    const int pw = warp;
     const uint64_t pol_k = ptx::policy_evict_first();
     const uint64_t pol_q = ptx::policy_evict_last();
     const int P = p.page_size;
-    const int ppt = P >= kTile ? 1 : kTile / P;          // pages per tile
+    const int ppt = P >= kTile ? 1 : kTile / P;          // pages per tile (<= 16)
+    const int log2p = __ffs(P) - 1;                      // P is a power of two
     const int tok_per_box = P >= kTile ? kTile : P;
     const uint32_t box_bytes = (uint32_t)tok_per_box * kTokenBytes;
-    CtxCache cc;
-    int b = pt.b0, t = pt.t0;
-    int64_t raw = pt.n_tiles > 0 ? cc.get(p, b, lane) : 0;
-    int64_t ce = ctx_eff(raw, p.cap), nt = req_tiles(ce);
-    int q_count = 0;
-    // page ids of the current tile (one lane per page)
-    auto page_of = [&](int bb, int tt, int64_t cee) -> int64_t {
-      const int64_t tok0 = (int64_t)tt * kTile + (P >= kTile ? 0 : (int64_t)lane * P);
-      if (lane >= ppt || tok0 >= cee) return -2;                          // not needed
-      return (int64_t)p.block_table[(int64_t)bb * p.bt_stride + tok0 / P];   // widened before use
+    const int pl = lane;                                 // page of the tile this lane serves
+    const int own = pt.n_tiles > pw ? (pt.n_tiles - pw + kProducers - 1) / kProducers : 0;
+    // Two cursors over this CTA's tiles: `cur` at this warp's tile being
+    // issued, `la` kLookahead own tiles ahead, whose page ids are copied into a
+    // shared-memory ring with cp.async so their latency overlaps the pipeline.
+    // q_seq counts the requests entered before `cur`'s (its Q slot is q_seq & 1).
+    // Warp 0 alone loads Q, for every request in order as its cursor crosses
+    // request starts (its own tiles' and the other warps'): waiting on a Q
+    // slot's release in sequence keeps each parity wait unambiguous.
+    CtxCache cc, cc_la;
+    Cursor cur, la;
+    int q_seq = 0, ci = 0;                               // ci: tile index of `cur`
+    bool qok = true;
+    auto issue_q = [&](int b, int seq) {
+      const int qs = seq & 1;
+      if (!ptx::mbar_wait_warp(qempty(qs), ((uint32_t)(seq >> 1) & 1u) ^ 1u, abort_flag, kWaitBudget)) {
+        qok = false;
+        if (lane == 0) fail();
+        return;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(qfull(qs), K::Q_BYTES);
+        for (int x = 0; x < K::N / K::QBOX; ++x)
+          ptx::tma_load_2d(s_q + qs * K::Q_BYTES + x * K::QBOX * kHeadDim, &tmap_q, 0, b * K::N + x * K::QBOX,
+                           qfull(qs), pol_q);
+      }
     };
-    int64_t pg = pt.n_tiles > 0 ? page_of(b, t, ce) : -2;
+    // Advance `cur` one tile; warp 0 loads Q for a request it enters.
+    auto step = [&]() {
+      const int entered = cur.advance(p, cc, lane);
+      ++ci;
+      q_seq += entered;
+      if (entered && pw == 0 && qok) issue_q(cur.b, q_seq);
+    };
+    if (own > 0) {
+      cur.start(p, pt.b0, pt.t0, cc, lane);
+      if (pw == 0) issue_q(cur.b, 0);
+      for (int x = 0; x < pw; ++x) step();
+      la = cur;
+    }
+    const uint32_t ring = s_base + L.ids + (uint32_t)(pw * kLookahead * 32 * 4);
+    const int32_t* ring_ptr = reinterpret_cast<const int32_t*>(smem + L.ids) + pw * kLookahead * 32;
+    int la_j = 0;
+    auto issue_ids = [&]() {
+      if (la_j < own) {
+        const int64_t tok0 = (int64_t)la.t * kTile + (P >= kTile ? 0 : (int64_t)lane * P);
+        const bool v = lane < ppt && tok0 < la.ce;
+        const int32_t* src = p.block_table + (v ? (int64_t)la.b * p.bt_stride + (tok0 >> log2p) : 0);
+        ptx::cp_async_4(ring + (uint32_t)(((la_j % kLookahead) * 32 + lane) * 4), src, v ? 4u : 0u);
+        if (la_j + 1 < own)
+          for (int x = 0; x < kProducers; ++x) la.advance(p, cc_la, lane);
+        ++la_j;
+      }
+      ptx::cp_async_commit();
+    };
+    for (int k = 0; k < kLookahead; ++k) issue_ids();
     bool ok = true;
-    int i = 0;
-    for (; i < pt.n_tiles && ok; ++i) {
+    int j = 0;
+    for (; j < own && ok; ++j) {
+      const int i = pw + j * kProducers;
       const int s = i % stages;
       const uint32_t ph = (uint32_t)(i / stages) & 1u;
-      const bool is_new = (i == 0) || (t == 0);
-      const bool is_last = (t == nt - 1) || (i == pt.n_tiles - 1);
-      // next tile's coordinates and page ids, loaded ahead of the waits
-      int bn = b, tn = t + 1;
-      int64_t rawn = raw, cen = ce, ntn = nt;
-      if (tn == nt && i + 1 < pt.n_tiles) {
-        do {
-          ++bn;
-          rawn = cc.get(p, bn, lane);
-          cen = ctx_eff(rawn, p.cap);
-          ntn = req_tiles(cen);
-        } while (ntn == 0 && bn + 1 < p.batch);
-        tn = 0;
-      }
-      const int64_t pg_next = (i + 1 < pt.n_tiles) ? page_of(bn, tn, cen) : -2;
-
-      if (is_new) {
-        const int qs = q_count & 1;
-        if (!ptx::mbar_wait_warp(qempty(qs), ((uint32_t)(q_count >> 1) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(qfull(qs), K::Q_BYTES);
-          for (int x = 0; x < K::N / K::QBOX; ++x)
-            ptx::tma_load_2d(s_q + qs * K::Q_BYTES + x * K::QBOX * kHeadDim, &tmap_q, 0, b * K::N + x * K::QBOX,
-                             qfull(qs), pol_q);
-        }
-        ++q_count;
-      }
+      const bool is_new = (i == 0) || (cur.t == 0);
+      const bool is_last = (cur.t == cur.nt - 1) || (i == pt.n_tiles - 1);
+      const int qs = q_seq & 1;
+      if (!qok) { ok = false; break; }
       if (!ptx::mbar_wait_warp(kempty(s), ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
-      const bool need = pg != -2;
+      ptx::cp_async_wait<kLookahead - 1>();                  // page ids of this tile have landed
+      const int64_t tok0 = (int64_t)cur.t * kTile + (P >= kTile ? 0 : (int64_t)pl * P);
+      const bool need = pl < ppt && tok0 < cur.ce;
+      const int64_t pg = (int64_t)ring_ptr[(j % kLookahead) * 32 + pl];   // widened before use
       const bool bad = need && (pg < 0 || pg >= p.num_pages);
       const bool load = need && !bad;
       const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
       if (bad) {
-        for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : lane * P) + x] = __int_as_float(0x7fc00000);
+        for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
         ptx::fence_proxy_async_smem();
         raise_status(p.status, SAI_STATUS_BAD_PAGE);
       }
       if (lane == 0) {
-        meta[s] = make_int4(b, t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, raw)),
-                            (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (((q_count - 1) & 1) << 8));
+        meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
+                            (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes);
       __syncwarp();
       if (load) {
-        const int y = P > kTile ? (t & 1) * kTile : 0;                           // half of a 256-token page
-        const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : lane * P * kHeadDim);
+        const int y = P > kTile ? (cur.t & 1) * kTile : 0;                       // half of a 256-token page
+        const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : pl * P * kHeadDim);
         ptx::tma_load_3d(dst, &tmap_kv, 0, y, (int)pg, full(s), pol_k);
         const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)P * kHeadDim + (int64_t)y * kScaleBytes;
-        const uint32_t sdst = s_base + L.sc + s * kScaleSlot + (P >= kTile ? 0 : lane * P * kScaleBytes);
+        const uint32_t sdst = s_base + L.sc + s * kScaleSlot + (P >= kTile ? 0 : pl * P * kScaleBytes);
         ptx::bulk_load(sdst, src, (uint32_t)tok_per_box * kScaleBytes, full(s), pol_k);
       }
-      b = bn; t = tn; raw = rawn; ce = cen; nt = ntn; pg = pg_next;
+      __syncwarp();
+      issue_ids();                                             // refill the slot just read
+      if (j + 1 < own)
+        for (int x = 0; x < kProducers; ++x) step();
     }
+    // Warp 0 still loads Q for requests that start in the other warps' last tiles.
+    if (pw == 0 && ok && own > 0)
+      while (ci + 1 < pt.n_tiles && qok) step();
+    ok = ok && qok;
+    ptx::cp_async_wait<0>();
     if (!ok) {
-      // Let the copies already issued land before the CTA exits.
+      // Let this warp's copies already issued land before the CTA exits.
       const int zero_flag = 0;
-      for (int k2 = max(0, i - stages); k2 < i; ++k2)
-        ptx::mbar_wait_warp(full(k2 % stages), (uint32_t)(k2 / stages) & 1u, &zero_flag, 1LL << 26);
+      const int i_end = pw + j * kProducers;
+      for (int k2 = max(0, i_end - stages); k2 < i_end; ++k2)
+        if (k2 % kProducers == pw)
+          ptx::mbar_wait_warp(full(k2 % stages), (uint32_t)(k2 / stages) & 1u, &zero_flag, 1LL << 26);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issuer -------------------------------------------------------------
     if (lane == 0) {
       int q_count = 0, acc_count = 0;
@@ -393,7 +511,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     __syncwarp();
   } else {
     // ---- epilogue ---------------------------------------------------------------
-    const int ew = warp - 2;
+    const int ew = warp - kFirstEpiWarp;
     const int wg = ew >> 2;
     const int quarter = warp & 3;                 // TMEM lanes this warp may read
     const int token = quarter * 32 + lane;
@@ -486,7 +604,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   // ---- tear-down ----------------------------------------------------------------
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, K::TMEM_COLS);
   }
@@ -538,10 +656,7 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int per_stage = kStageBytes + kScaleSlot + 16 + 16;
-  const int fixed = 1024 + 2 * K::Q_BYTES + 8 * (4 + 2 * K::ACC + 1) + 64;
-  const int stages = min(8, (kMaxSmem - fixed) / per_stage);
-  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC);
+  const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC);
   const size_t smem = (size_t)L.total + 1024;
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H>, smem, smem_set);
@@ -552,10 +667,23 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   p.kv = a.kv; p.num_pages = a.num_pages; p.page_size = P; p.weights = a.weights;
   p.logits = a.logits; p.stride = a.stride; p.width = a.width;
   p.cap = min(a.width, a.bt_stride * (int64_t)P);
-  p.batch = a.batch; p.stages = stages; p.status = a.status;
+  p.batch = a.batch; p.status = a.status;
   const int grid = device_sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  logits_tc_kernel<NEXT_N, H><<<grid, kThreadsTc, smem, stream>>>(tkv, tq, p);
+  // Programmatic dependent launch: the CTAs may be scheduled (barrier set-up,
+  // TMEM allocation) while the previous kernel in the stream drains.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H>, tkv, tq, p);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
