@@ -143,33 +143,59 @@ __device__ __forceinline__ int64_t req_units(int64_t ce, int64_t W) {
   return (int64_t)NEXT_N * ((W - fs + kFillCols - 1) / kFillCols);
 }
 
+// Balanced split of n units over g parts: part i gets [begin(i), begin(i + 1)).
+__device__ __forceinline__ int64_t split_begin(int64_t n, int64_t g, int64_t i) {
+  const int64_t q = n / g, r = n % g;
+  return q * i + (i < r ? i : r);
+}
+
 // Warp 0: split the tiles and the fill units of all requests evenly across
-// the grid and locate this CTA's first tile and first unit.  Up to
-// 32 * kCtxRegs context lengths are read once into registers (one round of
-// loads in flight); longer batches are read in two passes.
+// the grid and locate this CTA's first tile and first fill unit.  For up to
+// 32 * kCtxRegs requests, lane l reads requests [l * R, (l + 1) * R) once
+// (R = ceil(batch / 32)) and one warp scan over the lane totals places every
+// request; larger batches are scanned 32 requests at a time.
 constexpr int kCtxRegs = 16;
 
 template <int NEXT_N>
 __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
-  const bool in_regs = p.batch <= 32 * kCtxRegs;
-  int64_t ce_r[kCtxRegs];
-  int64_t T = 0, U = 0;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
+  int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
+  int64_t tb = 0, te = 0, ub = 0, ue = 0;
   bool clamped = false;
-  if (in_regs) {
-    int32_t raw_r[kCtxRegs];
+  if (p.batch <= 32 * kCtxRegs) {
+    const int R = (p.batch + 31) / 32;
+    int32_t tl[kCtxRegs], ul[kCtxRegs];
+    int64_t lt = 0, lu = 0;
 #pragma unroll
     for (int x = 0; x < kCtxRegs; ++x) {
-      const int b = x * 32 + lane;
-      raw_r[x] = b < p.batch ? p.context_lens[b] : 0;
+      const int b = lane * R + x;
+      const bool v = x < R && b < p.batch;
+      const int64_t raw = v ? (int64_t)p.context_lens[b] : 0;
+      clamped |= v && (raw < 0 || raw > p.cap);
+      const int64_t ce = ctx_eff(raw, p.cap);
+      tl[x] = (int32_t)req_tiles(ce);
+      ul[x] = v ? (int32_t)req_units<NEXT_N>(ce, p.width) : 0;
+      lt += tl[x];
+      lu += ul[x];
     }
+    const int64_t it = warp_incl_scan64(lt, lane), iu = warp_incl_scan64(lu, lane);
+    const int64_t T = __shfl_sync(0xffffffffu, it, 31), U = __shfl_sync(0xffffffffu, iu, 31);
+    tb = split_begin(T, G, cta); te = split_begin(T, G, cta + 1);
+    ub = split_begin(U, G, cta); ue = split_begin(U, G, cta + 1);
+    int fb = -1, ft = 0, gb = -1, gu = 0;
+    int64_t at = it - lt, au = iu - lu;              // units before this lane's first request
 #pragma unroll
     for (int x = 0; x < kCtxRegs; ++x) {
-      clamped |= raw_r[x] < 0 || raw_r[x] > p.cap;
-      ce_r[x] = ctx_eff(raw_r[x], p.cap);
-      T += req_tiles(ce_r[x]);
-      U += req_units<NEXT_N>(ce_r[x], p.width);
+      if (tl[x] > 0 && at <= tb && tb < at + tl[x]) { fb = lane * R + x; ft = (int)(tb - at); }
+      if (ul[x] > 0 && au <= ub && ub < au + ul[x]) { gb = lane * R + x; gu = (int)(ub - au); }
+      at += tl[x];
+      au += ul[x];
     }
+    const uint32_t bt = __ballot_sync(0xffffffffu, fb >= 0), bu = __ballot_sync(0xffffffffu, gb >= 0);
+    if (bt) { b0 = __shfl_sync(0xffffffffu, fb, __ffs(bt) - 1); t0 = __shfl_sync(0xffffffffu, ft, __ffs(bt) - 1); }
+    if (bu) { fb0 = __shfl_sync(0xffffffffu, gb, __ffs(bu) - 1); fu0 = __shfl_sync(0xffffffffu, gu, __ffs(bu) - 1); }
   } else {
+    int64_t T = 0, U = 0;
     for (int b = lane; b < p.batch; b += 32) {
       const int64_t raw = p.context_lens[b];
       clamped |= raw < 0 || raw > p.cap;
@@ -177,48 +203,38 @@ __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
       T += req_tiles(ce);
       U += req_units<NEXT_N>(ce, p.width);
     }
-  }
-  T = warp_sum64(T);
-  U = warp_sum64(U);
-  if (blockIdx.x == 0 && __any_sync(0xffffffffu, clamped) && lane == 0) raise_status(p.status, SAI_STATUS_CTX_CLAMPED);
-  const int64_t G = gridDim.x, i = blockIdx.x;
-  const int64_t tb = T * i / G, te = T * (i + 1) / G;
-  const int64_t ub = U * i / G, ue = U * (i + 1) / G;
-  int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
-  int64_t ct = 0, cu = 0;
-  bool got_t = tb >= te, got_u = ub >= ue;
-  auto step = [&](int b, int64_t ce) {
-    const int64_t x = b < p.batch ? req_tiles(ce) : 0;
-    const int64_t y = b < p.batch ? req_units<NEXT_N>(ce, p.width) : 0;
-    const int64_t xi = warp_incl_scan64(x, lane), yi = warp_incl_scan64(y, lane);
-    const bool ht = !got_t && x > 0 && ct + xi - x <= tb && tb < ct + xi;
-    const bool hu = !got_u && y > 0 && cu + yi - y <= ub && ub < cu + yi;
-    const uint32_t bt = __ballot_sync(0xffffffffu, ht), bu = __ballot_sync(0xffffffffu, hu);
-    if (bt) {
-      const int src = __ffs(bt) - 1;
-      b0 = __shfl_sync(0xffffffffu, b, src);
-      t0 = (int)__shfl_sync(0xffffffffu, tb - (ct + xi - x), src);
-      got_t = true;
-    }
-    if (bu) {
-      const int src = __ffs(bu) - 1;
-      fb0 = __shfl_sync(0xffffffffu, b, src);
-      fu0 = (int)__shfl_sync(0xffffffffu, ub - (cu + yi - y), src);
-      got_u = true;
-    }
-    ct += __shfl_sync(0xffffffffu, xi, 31);
-    cu += __shfl_sync(0xffffffffu, yi, 31);
-  };
-  if (in_regs) {
-#pragma unroll
-    for (int x = 0; x < kCtxRegs; ++x)
-      if (x * 32 < p.batch && !(got_t && got_u)) step(x * 32 + lane, ce_r[x]);
-  } else {
+    T = warp_sum64(T);
+    U = warp_sum64(U);
+    tb = split_begin(T, G, cta); te = split_begin(T, G, cta + 1);
+    ub = split_begin(U, G, cta); ue = split_begin(U, G, cta + 1);
+    int64_t ct = 0, cu = 0;
+    bool got_t = tb >= te, got_u = ub >= ue;
     for (int base = 0; base < p.batch && !(got_t && got_u); base += 32) {
       const int b = base + lane;
-      step(b, b < p.batch ? ctx_eff(p.context_lens[b], p.cap) : 0);
+      const int64_t ce = b < p.batch ? ctx_eff(p.context_lens[b], p.cap) : 0;
+      const int64_t x = b < p.batch ? req_tiles(ce) : 0;
+      const int64_t y = b < p.batch ? req_units<NEXT_N>(ce, p.width) : 0;
+      const int64_t xi = warp_incl_scan64(x, lane), yi = warp_incl_scan64(y, lane);
+      const bool ht = !got_t && x > 0 && ct + xi - x <= tb && tb < ct + xi;
+      const bool hu = !got_u && y > 0 && cu + yi - y <= ub && ub < cu + yi;
+      const uint32_t bt = __ballot_sync(0xffffffffu, ht), bu = __ballot_sync(0xffffffffu, hu);
+      if (bt) {
+        const int src = __ffs(bt) - 1;
+        b0 = __shfl_sync(0xffffffffu, b, src);
+        t0 = (int)__shfl_sync(0xffffffffu, tb - (ct + xi - x), src);
+        got_t = true;
+      }
+      if (bu) {
+        const int src = __ffs(bu) - 1;
+        fb0 = __shfl_sync(0xffffffffu, b, src);
+        fu0 = (int)__shfl_sync(0xffffffffu, ub - (cu + yi - y), src);
+        got_u = true;
+      }
+      ct += __shfl_sync(0xffffffffu, xi, 31);
+      cu += __shfl_sync(0xffffffffu, yi, 31);
     }
   }
+  if (blockIdx.x == 0 && __any_sync(0xffffffffu, clamped) && lane == 0) raise_status(p.status, SAI_STATUS_CTX_CLAMPED);
   if (lane == 0) {
     part->b0 = b0; part->t0 = t0; part->n_tiles = (int)(te - tb);
     part->fb0 = fb0; part->fu0 = fu0; part->n_units = (int)(ue - ub);
@@ -291,6 +307,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   const uint32_t drain = bar + 8u * (2 * stages + 4 + 2 * K::ACC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  int* fill_next = reinterpret_cast<int*>(smem + L.misc + 8);      // next -inf fill unit to take
   Part* part = reinterpret_cast<Part*>(smem + L.misc + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,7 +326,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
         ptx::mbar_init(full(s), 1);
-        ptx::mbar_init(kempty(s), 1 + 4 * K::C);
+        ptx::mbar_init(kempty(s), 4 * K::C);   // every epilogue warp of the tile's jobs
       }
       for (int q = 0; q < 2; ++q) {
         ptx::mbar_init(qfull(q), 1);
@@ -321,6 +338,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
       ptx::mbar_init(drain, 1);
       *abort_flag = 0;
+      *fill_next = 0;
       ptx::fence_barrier_init();
     }
     __syncwarp();
@@ -497,7 +515,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           ptx::mma_commit(tfull(a));
         }
         if (!ok) { fail(); aborted = true; break; }
-        ptx::mma_commit(kempty(s));
+        // The stage is released by the epilogue warps of its jobs, each after
+        // its accumulator is complete, hence after every MMA reading the stage.
         if (m.w & kFlagLast) ptx::mma_commit(qempty(qs));
       }
       // After an abort, the MMAs already issued complete before TMEM is freed
@@ -520,29 +539,35 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     for (int a = wg; a < jobs; a += 2) {
       const int i = a / K::C, c = a % K::C, s = i % stages;
       const int acc = a % K::ACC;
-      if (!ptx::mbar_wait_warp(tfull(acc), (uint32_t)(a / K::ACC) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
+      // The stage's data (and its meta) first: the first weights can then be
+      // read while the MMA of this job completes.
       if (!ptx::mbar_wait_warp(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
       const int4 m = meta[s];
       const float sc = scales[s * kTile + token];
+      const float4* w0 = reinterpret_cast<const float4*>(p.weights + ((int64_t)m.x * NEXT_N + c * K::ROWS) * H);
+      float4 wn[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) wn[x] = __ldg(w0 + x);
+      if (!ptx::mbar_wait_warp(tfull(acc), (uint32_t)(a / K::ACC) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(kempty(s));
       ptx::tc_fence_after();
       float out[K::ROWS];
 #pragma unroll
       for (int jr = 0; jr < K::ROWS; ++jr) {
-        const int j = c * K::ROWS + jr;
-        const float4* wrow = reinterpret_cast<const float4*>(p.weights + ((int64_t)m.x * NEXT_N + j) * H);
+        const float4* wrow = w0 + jr * (H / 4);
         float accum = 0.f;
 #pragma unroll
-        for (int h0 = 0; h0 < H; h0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32(t_lane + (uint32_t)(acc * K::NC + jr * H + h0), v);
-          float4 w4[8];
+        for (int h0 = 0; h0 < H; h0 += 64) {         // two 32-column TMEM loads, one wait
+          uint32_t v[64];
+          ptx::tmem_ld_32(t_lane + (uint32_t)(acc * K::NC + jr * H + h0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          ptx::tmem_ld_32(t_lane + (uint32_t)(acc * K::NC + jr * H + h0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          float4 w4[16];
 #pragma unroll
-          for (int x = 0; x < 8; ++x) w4[x] = __ldg(wrow + (h0 >> 2) + x);
+          for (int x = 0; x < 16; ++x) w4[x] = (jr == 0 && h0 == 0 && x < 8) ? wn[x] : __ldg(wrow + (h0 >> 2) + x);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
+          for (int x = 0; x < 16; ++x) {
             accum = fmaf(w4[x].x, fmaxf(__uint_as_float(v[4 * x + 0]), 0.f), accum);
             accum = fmaf(w4[x].y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), accum);
             accum = fmaf(w4[x].z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), accum);
@@ -565,39 +590,48 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         }
       }
     }
-    // ---- -inf fill past each request's last tile ------------------------------
+  }
+
+  // ---- -inf fill past each request's last tile --------------------------------
+  // Every warp takes units from a shared counter once its role is done, so the
+  // warps that finish first (the producers) do most of it.
+  {
     CtxCache cc;
     int b = pt.fb0;
-    int64_t u_in = pt.fu0;
+    int64_t u_in = pt.fu0, ucur = 0;
     int64_t ce = pt.n_units > 0 ? ctx_eff(cc.get(p, b, lane), p.cap) : 0;
     int64_t fs = min(p.width, req_tiles(ce) * kTile);
     int64_t chunks = (p.width - fs + kFillCols - 1) / kFillCols;
-    for (int u = 0; u < pt.n_units; ++u) {
-      while (u_in >= NEXT_N * chunks && b < p.batch) {   // move to the next request with fill
+    for (;;) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(fill_next, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= pt.n_units) break;
+      u_in += u - ucur;                                // units only move forward for a warp
+      ucur = u;
+      while (u_in >= NEXT_N * chunks && b < p.batch) {   // move to the request holding unit u
+        u_in -= NEXT_N * chunks;
         ++b;
-        u_in = 0;
+        if (b >= p.batch) break;
         ce = ctx_eff(cc.get(p, b, lane), p.cap);
         fs = min(p.width, req_tiles(ce) * kTile);
         chunks = (p.width - fs + kFillCols - 1) / kFillCols;
       }
       if (b >= p.batch) break;                          // never past the last row
-      if (u % kEpiWarps == ew) {
-        const int j = (int)(u_in / chunks);
-        const int64_t c0 = fs + (u_in % chunks) * kFillCols;
-        const int64_t c1 = min(p.width, c0 + kFillCols);
-        float* row = p.logits + ((int64_t)b * NEXT_N + j) * p.stride;    // 64-bit row base
-        int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(row + c0) & 15)) & 15) >> 2);
-        head = min(head, c1 - c0);
-        if (lane < head) row[c0 + lane] = -INFINITY;
-        const int64_t v0 = c0 + head;
-        const int64_t nv = (c1 - v0) >> 2;
-        float4* vrow = reinterpret_cast<float4*>(row + v0);
-        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int64_t x = lane; x < nv; x += 32) vrow[x] = ninf;
-        const int64_t tail0 = v0 + nv * 4;
-        if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
-      }
-      ++u_in;
+      const int j = (int)(u_in / chunks);
+      const int64_t c0 = fs + (u_in % chunks) * kFillCols;
+      const int64_t c1 = min(p.width, c0 + kFillCols);
+      float* row = p.logits + ((int64_t)b * NEXT_N + j) * p.stride;    // 64-bit row base
+      int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(row + c0) & 15)) & 15) >> 2);
+      head = min(head, c1 - c0);
+      if (lane < head) row[c0 + lane] = -INFINITY;
+      const int64_t v0 = c0 + head;
+      const int64_t nv = (c1 - v0) >> 2;
+      float4* vrow = reinterpret_cast<float4*>(row + v0);
+      const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      for (int64_t x = lane; x < nv; x += 32) vrow[x] = ninf;
+      const int64_t tail0 = v0 + nv * 4;
+      if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
     }
   }
 
