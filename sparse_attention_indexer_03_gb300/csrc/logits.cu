@@ -40,6 +40,8 @@
 // TMEM and exits.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -491,14 +493,14 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       bool aborted = false;
       for (int i = 0; i < pt.n_tiles; ++i) {
         const int s = i % stages;
+        // The stage and Q barriers are completed by TMA, not by tcgen05
+        // operations, so no tcgen05 fence is needed after these two waits.
         if (!ptx::mbar_wait(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
-        ptx::tc_fence_after();
         const int4 m = meta[s];
         const int qs = (m.w >> 8) & 1;
         if (m.w & kFlagNew) {
           if (!ptx::mbar_wait(qfull(qs), (uint32_t)(q_count >> 1) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
           ++q_count;
-          ptx::tc_fence_after();
         }
         bool ok = true;
 #pragma unroll 1
@@ -649,6 +651,57 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Encoded tensor maps keyed by (base, rows, box, rank): a decode loop calls
+// with the same buffers every step and skips re-encoding.  The map depends
+// only on the key, so a hit is always valid; entries are replaced round-robin.
+struct TmapKey {
+  const void* base;
+  uint64_t extent;
+  uint32_t box;
+  uint32_t rank;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && extent == o.extent && box == o.box && rank == o.rank;
+  }
+};
+
+constexpr int kTmapCache = 32;
+struct TmapCache {
+  std::mutex mu;
+  TmapKey keys[kTmapCache] = {};
+  CUtensorMap maps[kTmapCache];
+  int dev[kTmapCache] = {};
+  int next = 0;
+};
+
+TmapCache& tmap_cache() {
+  static TmapCache c;
+  return c;
+}
+
+bool tmap_lookup(const TmapKey& k, CUtensorMap* out) {
+  int d = 0;
+  cudaGetDevice(&d);
+  TmapCache& c = tmap_cache();
+  std::lock_guard<std::mutex> g(c.mu);
+  for (int i = 0; i < kTmapCache; ++i)
+    if (c.keys[i].base != nullptr && c.keys[i] == k && c.dev[i] == d) {
+      *out = c.maps[i];
+      return true;
+    }
+  return false;
+}
+
+void tmap_store(const TmapKey& k, const CUtensorMap& m) {
+  int d = 0;
+  cudaGetDevice(&d);
+  TmapCache& c = tmap_cache();
+  std::lock_guard<std::mutex> g(c.mu);
+  c.keys[c.next] = k;
+  c.maps[c.next] = m;
+  c.dev[c.next] = d;
+  c.next = (c.next + 1) % kTmapCache;
+}
+
 EncodeTiled encode_fn() {
   static EncodeTiled fn = nullptr;
   if (fn == nullptr) {
@@ -670,25 +723,33 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   const int P = a.page_size;
   CUtensorMap tkv, tq;
   {
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)P,
-                                (cuuint64_t)(a.num_pages < (int64_t)INT32_MAX ? a.num_pages : (int64_t)INT32_MAX)};
-    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)P * kTokenBytes};
-    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)min(P, kTile), 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    const uint64_t np = (uint64_t)(a.num_pages < (int64_t)INT32_MAX ? a.num_pages : (int64_t)INT32_MAX);
+    const TmapKey key{a.kv, np, (uint32_t)P, 3};
+    if (!tmap_lookup(key, &tkv)) {
+      const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)P, (cuuint64_t)np};
+      const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)P * kTokenBytes};
+      const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)min(P, kTile), 1};
+      const cuuint32_t es[3] = {1, 1, 1};
+      if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+      tmap_store(key, tkv);
+    }
   }
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.batch * K::N};
-    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
-    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)K::QBOX};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    const TmapKey key{a.q, (uint64_t)a.batch * K::N, (uint32_t)K::QBOX, 2};
+    if (!tmap_lookup(key, &tq)) {
+      const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.batch * K::N};
+      const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+      const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)K::QBOX};
+      const cuuint32_t es[2] = {1, 1};
+      if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.q), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+      tmap_store(key, tq);
+    }
   }
   const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC);
   const size_t smem = (size_t)L.total + 1024;
