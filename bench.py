@@ -103,10 +103,10 @@ def source_sha(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, fused: bool = False):
     """DRAM bytes per logits launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"logits_tc_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"logits_tc{'_topk' if fused else ''}_{workload}.md")
     src = os.path.join(ROOT, "sparse_attention_indexer_03_gb300", "csrc", "logits.cu")
     if not os.path.exists(path):
         return None
@@ -265,16 +265,33 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         d = w.to_device(dev)
         d["logits"] = torch.empty((w.rows, w.logits_stride), dtype=torch.float32, device=dev)
         d["indices"] = torch.empty((w.rows, w.topk), dtype=torch.int32, device=dev)
+        d["ws"] = torch.zeros(max(1, w.batch), dtype=torch.int32, device=dev)
         sets.append(d)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(d):
+    fused = args.path == "fused"
+
+    def logits_call(d):
         sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
                              d["block_table"], d["logits"], w.max_model_len, num_pages=w.pool.num_pages,
                              status=status, stream=stream)
+
+    def topk_call(d):
         sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
                                  d["indices"], stream=stream)
+
+    def fused_call(d):
+        sai.paged_mqa_logits_topk(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
+                                  d["block_table"], d["logits"], w.max_model_len, w.topk, d["indices"],
+                                  d["ws"], num_pages=w.pool.num_pages, status=status, stream=stream)
+
+    def step(d):
+        if fused:
+            fused_call(d)
+        else:
+            logits_call(d)
+            topk_call(d)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -306,12 +323,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             for i in range(S):
                 d = sets[i % R]
                 ev[i][0].record(stream)
-                sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
-                                     d["block_table"], d["logits"], w.max_model_len, num_pages=w.pool.num_pages,
-                                     status=status, stream=stream)
+                fused_call(d) if fused else logits_call(d)
                 ev[i][1].record(stream)
-                sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
-                                         d["indices"], stream=stream)
+                if not fused:
+                    topk_call(d)
                 ev[i][2].record(stream)
     with torch.cuda.stream(stream):
         graph.replay()                  # untimed: graph upload and warm-up
@@ -346,12 +361,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 a, b2, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
                 d = sets[i % R]
                 a.record(stream)
-                sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
-                                     d["block_table"], d["logits"], w.max_model_len,
-                                     num_pages=w.pool.num_pages, status=status, stream=stream)
+                fused_call(d) if fused else logits_call(d)
                 b2.record(stream)
-                sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
-                                         d["indices"], stream=stream)
+                if not fused:
+                    topk_call(d)
                 c.record(stream)
                 torch.cuda.synchronize()
                 logits_ms.append(a.elapsed_time(b2))
@@ -388,7 +401,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     peaks = load_peaks()
     lg_ms = float(np.mean(logits_ms))
     tk_ms = float(np.mean(topk_ms))
-    lbytes = logits_bytes(w)
+    # The fused kernel's compulsory HBM bytes add the index rows it writes;
+    # the logits it selects from are re-read through L2.
+    lbytes = logits_bytes(w) + (w.rows * w.topk * 4 if fused else 0)
     lflops = logits_flops(w)
     fp8_peak_tflops = 2.0 * peaks["bf16_tflops"]          # nominal fp8 : bf16 dense ratio 4.5 : 2.25
     t_hbm = lbytes / (peaks["hbm_gbs"] * 1e9)
@@ -400,8 +415,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         roof = {"bound": "tensor", "achieved": lflops / (lg_ms * 1e-3) / 1e12, "peak": fp8_peak_tflops,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic(w.name)
-    roof["kernel"] = "logits_tc_kernel"
+    roof["traffic"] = profiled_traffic(w.name, fused)
+    roof["kernel"] = "logits_tc_kernel" + (" (fused top-k)" if fused else "")
     roof["algorithmic_per_launch"] = lbytes if roof["bound"] == "hbm" else lflops
     roof["peak_source"] = peaks["source"] + (" (fp8 = 2 x measured bf16)" if roof["bound"] == "tensor" else "")
     value = tok_all * K / (ms * 1e-3) / 1e9
@@ -420,14 +435,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "l2": f"{R} rotating input sets, {R * touched / 2**20:.0f} MB touched per cycle > 129 MB L2",
                        "timing": f"{K // S} replays of a CUDA graph of {S} steps; kernel durations from "
                                  f"a replay of the same steps with timing events around each kernel",
-                       "logits_ms": lg_ms, "topk_ms": tk_ms,
-                       "topk_gbs": topk_bytes(w) / (tk_ms * 1e-3) / 1e9,
+                       "path": ("one fused launch (logits, then top-k by the CTA completing each request)"
+                                if fused else "two launches (logits, top-k)"),
+                       "logits_ms": lg_ms, "topk_ms": None if fused else tk_ms,
+                       "topk_gbs": None if fused else topk_bytes(w) / (tk_ms * 1e-3) / 1e9,
                        "parallelism": f"replicas x{world} (independent requests per GPU)"},
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": tok_all * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * K,
+            "gpu_launches": (1 if fused else 2) * K,
             "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
     return 0
@@ -441,6 +458,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "separate"], default="separate",
+                    help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

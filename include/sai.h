@@ -62,7 +62,7 @@ typedef struct CUstream_st* sai_stream_t;
 #define SAI_ERR_INVALID_ARGUMENT (-1)  /* null pointer, negative size, stride < width, ... */
 #define SAI_ERR_UNSUPPORTED      (-2)  /* valid but not built: head_dim != 128, page size, ... */
 #define SAI_ERR_MISALIGNED       (-3)  /* a pointer lacks the alignment stated below */
-#define SAI_ERR_WORKSPACE        (-4)  /* top-k workspace missing or too small */
+#define SAI_ERR_WORKSPACE        (-4)  /* workspace missing or too small */
 #define SAI_ERR_CUDA             (-5)  /* a CUDA runtime call or kernel launch failed */
 
 /* Bits of the device status word (OR-ed in by kernels, never cleared). */
@@ -155,6 +155,47 @@ SAI_API int sai_top_k_per_row_decode(const float* logits, int64_t logits_stride,
                              int64_t max_model_len, int32_t k,
                              int32_t* indices, int64_t indices_stride,
                              void* workspace, size_t workspace_bytes, sai_stream_t stream);
+
+/*
+ * sai_paged_mqa_logits_topk_workspace_bytes -- bytes of device workspace that
+ * sai_paged_mqa_logits_topk needs for `batch` requests: one int32 counter per
+ * request (0 for batch < 0).
+ */
+SAI_API size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch);
+
+/*
+ * sai_paged_mqa_logits_topk -- logits and their per-row top-k in one launch.
+ *
+ * The two ops above, fused: the same logits are written to `logits` exactly
+ * as sai_paged_mqa_logits writes them, and `indices` receives what
+ * sai_top_k_per_row_decode would select from them, in the same order.  The
+ * arguments up to max_model_len, `status` and `stream` are those of
+ * sai_paged_mqa_logits, and k, indices and indices_stride those of
+ * sai_top_k_per_row_decode; only SAI_KV_PAGE_SPLIT caches are accepted.
+ * Row r's top-k runs over its ctx_r columns, ctx_r clamped as for the logits
+ * (to min(max_model_len, block_table_stride * page_size)).
+ *
+ *   workspace       device, >= sai_paged_mqa_logits_topk_workspace_bytes(batch)
+ *                   bytes, 4-byte aligned, ALL ZERO before the first call.
+ *                   Each call leaves it all zero again, so it is zeroed once
+ *                   and reused; after a call that raised SAI_STATUS_TIMEOUT
+ *                   it must be zeroed again.  Two calls in flight at once
+ *                   (on different streams) must not share it.
+ *
+ * How the launch joins the two steps: each CTA, once its logits are stored,
+ * adds the number of tiles it computed for a request to that request's
+ * counter; the CTA whose addition completes the request selects the
+ * request's rows.  No CTA waits for another.
+ */
+SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache,
+                              int64_t num_pages, int32_t page_size,
+                              const float* weights, const int32_t* context_lens,
+                              const int32_t* block_table, int64_t block_table_stride,
+                              int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim,
+                              float* logits, int64_t logits_stride, int64_t max_model_len,
+                              int32_t k, int32_t* indices, int64_t indices_stride,
+                              void* workspace, size_t workspace_bytes,
+                              uint32_t* status, sai_stream_t stream);
 
 /* Static, human-readable name of a return code. */
 SAI_API const char* sai_error_string(int code);

@@ -9,6 +9,8 @@ computation runs in the library's CUDA kernels; there is no fallback.  If
     paged_mqa_logits(q, kv_cache, page_size, weights, context_lens, block_table,
                      logits, max_model_len, ...)
     top_k_per_row_decode(logits, context_lens, next_n, max_model_len, k, indices, ...)
+    paged_mqa_logits_topk(q, kv_cache, page_size, weights, context_lens, block_table,
+                          logits, max_model_len, k, indices, workspace, ...)
 """
 from __future__ import annotations
 
@@ -21,6 +23,7 @@ from . import _build
 __all__ = [
     "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
     "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
+    "logits_topk_workspace_bytes", "paged_mqa_logits_topk",
     "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
     "KV_PAGE_SPLIT", "KV_INTERLEAVED",
 ]
@@ -63,6 +66,11 @@ _SIGS = {
     "sai_top_k_workspace_bytes": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32]),
     "sai_top_k_per_row_decode": (_c.c_int, [_P, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int64,
                                             _c.c_int32, _P, _c.c_int64, _P, _c.c_size_t, _P]),
+    "sai_paged_mqa_logits_topk_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
+    "sai_paged_mqa_logits_topk": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int32, _P, _P, _P, _c.c_int64,
+                                             _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                             _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _c.c_int64,
+                                             _P, _c.c_size_t, _P, _P]),
     "sai_error_string": (_c.c_char_p, [_c.c_int]),
     "sai_version": (_c.c_int, []),
 }
@@ -127,19 +135,9 @@ def _ptr(t, dtype, name):
     return t.data_ptr()
 
 
-def paged_mqa_logits(q, kv_cache, page_size: int, weights, context_lens, block_table,
-                     logits, max_model_len: int, *, num_pages: Optional[int] = None,
-                     status=None, kv_layout="split", stream=None) -> None:
-    """FP8 paged MQA logits into `logits` (see `sai_paged_mqa_logits`).
-
-    q            uint8 or float8_e4m3fn [B, next_n, H, 128], contiguous
-    kv_cache     uint8 / float8 bytes of num_pages * page_size * 132 (any shape, contiguous)
-    weights      float32 [B * next_n, H], contiguous
-    context_lens int32 [B]
-    block_table  int32 [B, stride] (row stride from the tensor; inner stride 1)
-    logits       float32 [B * next_n, >= max_model_len] (row stride from the tensor)
-    status       optional int32/uint32-sized CUDA tensor of one element
-    """
+def _logits_args(q, kv_cache, page_size, weights, context_lens, block_table, logits, max_model_len,
+                 num_pages):
+    """Marshalled arguments shared by the logits entry points, up to max_model_len."""
     import torch
 
     u8 = (torch.uint8, torch.float8_e4m3fn)
@@ -155,16 +153,64 @@ def paged_mqa_logits(q, kv_cache, page_size: int, weights, context_lens, block_t
     page_bytes = page_size * (D + 4)
     if num_pages is None:
         num_pages = kv_cache.numel() * kv_cache.element_size() // page_bytes
+    return (_ptr(q, u8, "q"), _ptr(kv_cache, u8, "kv_cache"), int(num_pages), int(page_size),
+            _ptr(weights, torch.float32, "weights"), _ptr(context_lens, torch.int32, "context_lens"),
+            _ptr(block_table, torch.int32, "block_table"), int(block_table.stride(0)),
+            int(B), int(next_n), int(H), int(D),
+            _ptr(logits, torch.float32, "logits"), int(logits.stride(0)), int(max_model_len))
+
+
+def paged_mqa_logits(q, kv_cache, page_size: int, weights, context_lens, block_table,
+                     logits, max_model_len: int, *, num_pages: Optional[int] = None,
+                     status=None, kv_layout="split", stream=None) -> None:
+    """FP8 paged MQA logits into `logits` (see `sai_paged_mqa_logits`).
+
+    q            uint8 or float8_e4m3fn [B, next_n, H, 128], contiguous
+    kv_cache     uint8 / float8 bytes of num_pages * page_size * 132 (any shape, contiguous)
+    weights      float32 [B * next_n, H], contiguous
+    context_lens int32 [B]
+    block_table  int32 [B, stride] (row stride from the tensor; inner stride 1)
+    logits       float32 [B * next_n, >= max_model_len] (row stride from the tensor)
+    status       optional int32/uint32-sized CUDA tensor of one element
+    """
+    import torch
+
+    args = _logits_args(q, kv_cache, page_size, weights, context_lens, block_table, logits,
+                        max_model_len, num_pages)
     code = library().sai_paged_mqa_logits(
-        _ptr(q, u8, "q"), _ptr(kv_cache, u8, "kv_cache"), int(num_pages), int(page_size),
-        _ptr(weights, torch.float32, "weights"), _ptr(context_lens, torch.int32, "context_lens"),
-        _ptr(block_table, torch.int32, "block_table"), int(block_table.stride(0)),
-        int(B), int(next_n), int(H), int(D),
-        _ptr(logits, torch.float32, "logits"), int(logits.stride(0)), int(max_model_len),
-        int(_LAYOUTS[kv_layout]), _ptr(status, (torch.int32, torch.uint32), "status"),
+        *args, int(_LAYOUTS[kv_layout]), _ptr(status, (torch.int32, torch.uint32), "status"),
         _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_paged_mqa_logits")
+
+
+def logits_topk_workspace_bytes(batch: int) -> int:
+    return int(library().sai_paged_mqa_logits_topk_workspace_bytes(int(batch)))
+
+
+def paged_mqa_logits_topk(q, kv_cache, page_size: int, weights, context_lens, block_table,
+                          logits, max_model_len: int, k: int, indices, workspace, *,
+                          num_pages: Optional[int] = None, status=None, stream=None) -> None:
+    """Logits and per-row top-k in one launch (see `sai_paged_mqa_logits_topk`).
+
+    Arguments as `paged_mqa_logits` (page-split caches only) plus
+    indices    int32 [B * next_n, >= k] (row stride from the tensor)
+    workspace  CUDA tensor of >= logits_topk_workspace_bytes(B) bytes, zero
+               before the first call; every call leaves it zero again.
+    """
+    import torch
+
+    if indices.dim() != 2 or indices.stride(1) != 1:
+        raise ValueError("indices must be [rows, stride] with unit inner stride")
+    args = _logits_args(q, kv_cache, page_size, weights, context_lens, block_table, logits,
+                        max_model_len, num_pages)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    code = library().sai_paged_mqa_logits_topk(
+        *args, int(k), _ptr(indices, torch.int32, "indices"), int(indices.stride(0)),
+        _ptr(workspace, None, "workspace"), int(ws_bytes),
+        _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_paged_mqa_logits_topk")
 
 
 def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:

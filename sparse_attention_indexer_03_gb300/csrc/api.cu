@@ -48,12 +48,17 @@ const char* sai_error_string(int code) {
   }
 }
 
-int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
-                         const float* weights, const int32_t* context_lens, const int32_t* block_table,
-                         int64_t block_table_stride, int32_t batch, int32_t next_n, int32_t heads,
-                         int32_t head_dim, float* logits, int64_t logits_stride, int64_t max_model_len,
-                         int32_t kv_layout, uint32_t* status, sai_stream_t stream) {
-  using namespace sai;
+}  // extern "C"
+
+namespace sai {
+namespace {
+
+// Checks shared by the logits entry points; fills `a` on success.
+int check_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                 const float* weights, const int32_t* context_lens, const int32_t* block_table,
+                 int64_t block_table_stride, int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim,
+                 float* logits, int64_t logits_stride, int64_t max_model_len, int32_t kv_layout,
+                 uint32_t* status, LogitsArgs& a) {
   if (batch < 0 || next_n < 1 || heads < 1 || head_dim < 1 || page_size < 1 || num_pages < 1 ||
       block_table_stride < 1 || max_model_len < 1 || logits_stride < max_model_len)
     return SAI_ERR_INVALID_ARGUMENT;
@@ -69,19 +74,62 @@ int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t 
   if (!aligned(q_fp8, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) || !aligned(context_lens, 4) ||
       !aligned(block_table, 4) || !aligned(logits, 4) || !aligned(status, 4))
     return SAI_ERR_MISALIGNED;
-  if (batch == 0) return SAI_OK;
-
-  LogitsArgs a;
   a.q = q_fp8; a.kv = kv_cache; a.num_pages = num_pages; a.page_size = page_size;
   a.weights = weights; a.context_lens = context_lens; a.block_table = block_table;
   a.bt_stride = block_table_stride; a.batch = batch; a.next_n = next_n; a.heads = heads;
   a.logits = logits; a.stride = logits_stride; a.width = max_model_len; a.layout = kv_layout;
   a.status = status;
+  return SAI_OK;
+}
+
+}  // namespace
+}  // namespace sai
+
+extern "C" {
+
+int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                         const float* weights, const int32_t* context_lens, const int32_t* block_table,
+                         int64_t block_table_stride, int32_t batch, int32_t next_n, int32_t heads,
+                         int32_t head_dim, float* logits, int64_t logits_stride, int64_t max_model_len,
+                         int32_t kv_layout, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  LogitsArgs a;
+  const int rc = check_logits(q_fp8, kv_cache, num_pages, page_size, weights, context_lens, block_table,
+                              block_table_stride, batch, next_n, heads, head_dim, logits, logits_stride,
+                              max_model_len, kv_layout, status, a);
+  if (rc != SAI_OK || batch == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // Tensor cores for the page-split layout; its 132-byte token stride makes
   // the interleaved layout unreachable for tiled TMA, so it runs on the CUDA cores.
   if (kv_layout == SAI_KV_PAGE_SPLIT) return from_cuda(launch_logits_tc(a, st));
   return from_cuda(launch_logits_simt(a, st));
+}
+
+size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch) {
+  return batch < 0 ? 0 : (size_t)batch * sizeof(int32_t);
+}
+
+int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                              const float* weights, const int32_t* context_lens, const int32_t* block_table,
+                              int64_t block_table_stride, int32_t batch, int32_t next_n, int32_t heads,
+                              int32_t head_dim, float* logits, int64_t logits_stride, int64_t max_model_len,
+                              int32_t k, int32_t* indices, int64_t indices_stride, void* workspace,
+                              size_t workspace_bytes, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  LogitsArgs a;
+  const int rc = check_logits(q_fp8, kv_cache, num_pages, page_size, weights, context_lens, block_table,
+                              block_table_stride, batch, next_n, heads, head_dim, logits, logits_stride,
+                              max_model_len, SAI_KV_PAGE_SPLIT, status, a);
+  if (rc != SAI_OK) return rc;
+  if (k < 1 || indices_stride < k || !indices) return SAI_ERR_INVALID_ARGUMENT;
+  if (k > 65536 || max_model_len > INT32_MAX) return SAI_ERR_UNSUPPORTED;
+  if (indices_stride > (INT64_MAX / 8) / ((int64_t)batch * next_n + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if (!aligned(indices, 4) || !aligned(workspace, 4)) return SAI_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < (size_t)batch * sizeof(int32_t)) return SAI_ERR_WORKSPACE;
+  if (batch == 0) return SAI_OK;
+  a.indices = indices; a.idx_stride = indices_stride; a.k = k;
+  a.req_counter = static_cast<int32_t*>(workspace);
+  return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k) {

@@ -54,6 +54,11 @@ struct LogitsArgs {
   int64_t width;         // W = max_model_len
   int layout;
   uint32_t* status;
+  // fused top-k (indices null: logits only)
+  int32_t* indices = nullptr;
+  int64_t idx_stride = 0;
+  int k = 0;
+  int32_t* req_counter = nullptr;
 };
 
 cudaError_t launch_logits_simt(const LogitsArgs& a, cudaStream_t stream);
@@ -86,6 +91,11 @@ cudaError_t ensure_dynamic_smem(F* func, size_t bytes, int* done) {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && (size_t)done[dev] >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  // Every kernel of the library prefers the largest shared-memory carve-out,
+  // so consecutive launches (logits, then top-k) keep one SM configuration
+  // instead of reconfiguring the L1 / shared split between them.
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = (int)bytes;
   return e;
 }

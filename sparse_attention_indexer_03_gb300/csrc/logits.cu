@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "select.cuh"
 
 namespace sai {
 namespace {
@@ -77,6 +78,11 @@ struct TcParams {
   int64_t cap;          // min(W, bt_stride * P): longest context a row can have
   int batch;
   uint32_t* status;
+  // fused top-k (null indices: logits only)
+  int32_t* indices;
+  int64_t idx_stride;
+  int k;
+  int32_t* req_counter;   // [batch] tiles counted in so far, zero between launches
 };
 
 template <int NEXT_N, int H>
@@ -285,7 +291,112 @@ struct Cursor {
   }
 };
 
-template <int NEXT_N, int H>
+// ---- fused top-k: the CTA that completes a request selects its rows ---------
+// Each CTA adds, per request it touched, the number of that request's tiles it
+// processed to req_counter[b] once its logits are stored and fenced; the CTA
+// whose addition completes the request's tile count resets the counter to 0
+// and runs the top-k of the request's rows, reading them through L2.  No CTA
+// ever waits for another.  Requests without tiles get their -1 rows from CTA
+// (b mod grid).  Runs on the two epilogue warpgroups (256 threads, named
+// barrier 1); the drained K-stage ring holds the selection's histograms.
+constexpr int kFusedThreads = kEpiWarps * 32;
+constexpr int kOwnMax = 64;
+
+struct EpiBar {
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+};
+
+// `ring` is the drained part of shared memory (K stages and Q slots, `ring_bytes`
+// long): the histograms, the group's shared words, the list of requests to
+// select, then the keys of rows that fit (longer rows are re-read from L2).
+template <int NEXT_N>
+__device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int ring_bytes, int etid,
+                           const volatile int* abort_flag) {
+  constexpr int NT = kFusedThreads;
+  static_assert(NT == 256, "named barrier 1 counts 256 threads");
+  const EpiBar ebar;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ring);
+  auto* sh = reinterpret_cast<SelectShared<NT>*>(ring + kSelectSmem);
+  int* own = reinterpret_cast<int*>(ring + kSelectSmem + 512);   // [0] count (-1: stop), [1] more, [2..] requests
+  uint32_t* key_base = reinterpret_cast<uint32_t*>(ring + kSelectSmem + 1024);
+  const int key_cap = (ring_bytes - (int)kSelectSmem - 1024) / 4 - 3;
+  const int k = p.k;
+  __threadfence();                                   // this thread's logits are visible device-wide
+  ebar();
+  // The first warp walks this CTA's tiles 32 requests at a time: lane l takes
+  // request b + l, so one round trip of atomics covers 32 requests.
+  int b = pt.b0, left = pt.n_tiles;
+  int64_t t = pt.t0;
+  const int lane = etid & 31;
+  for (;;) {
+    if (etid < 32) {
+      int n_own = 0;
+      const bool stop = *abort_flag != 0;
+      while (!stop && left > 0 && n_own + 32 <= kOwnMax) {
+        const int bb = b + lane;
+        const int64_t nt = bb < p.batch ? req_tiles(ctx_eff(p.context_lens[bb], p.cap)) : 0;
+        const int64_t avail = lane == 0 ? nt - t : nt;
+        const int64_t incl = warp_incl_scan64(avail, lane);
+        const int64_t m = min(avail, max((int64_t)0, (int64_t)left - (incl - avail)));
+        bool mine = false;
+        if (m > 0) {
+          const int old = atomicAdd(&p.req_counter[bb], (int)m);
+          mine = (int64_t)old + m == nt;
+          if (mine) p.req_counter[bb] = 0;             // the last contributor restores zero
+        }
+        const uint32_t ob = __ballot_sync(0xffffffffu, mine);
+        if (mine) own[2 + n_own + __popc(ob & ((1u << lane) - 1u))] = bb;
+        n_own += __popc(ob);
+        const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total >= left) {
+          left = 0;
+        } else {
+          left -= (int)total;
+          b += 32;
+          t = 0;
+        }
+      }
+      if (lane == 0) {
+        own[0] = stop ? -1 : n_own;
+        own[1] = (!stop && left > 0) ? 1 : 0;
+      }
+      __threadfence();                               // the other CTAs' logits before the reads below
+    }
+    ebar();
+    const int n_own = own[0], more = own[1];
+    if (n_own < 0) return;                           // a wait timed out: leave the rest
+    for (int o = 0; o < n_own; ++o) {
+      const int bb = own[2 + o];
+      const int64_t raw = p.context_lens[bb];
+#pragma unroll 1
+      for (int j = 0; j < NEXT_N; ++j) {
+        const int64_t r = (int64_t)bb * NEXT_N + j;
+        const int64_t n = row_context(raw, NEXT_N, j, p.cap);
+        int32_t* out = p.indices + r * p.idx_stride;  // 64-bit row base
+        const float* row = p.logits + r * p.stride;
+        if (n <= k) {
+          for (int i = etid; i < k; i += NT) out[i] = i < n ? i : -1;
+        } else if (n <= key_cap) {
+          const uint32_t* keys = stage_keys<NT>(row, (int)n, key_base, etid);
+          topk_row_smem<NT>(keys, (int)n, k, out, *sh, hist, etid, ebar);
+        } else {
+          topk_row_stream<NT>(row, n, k, out, *sh, hist, etid, ebar);
+        }
+      }
+    }
+    ebar();                                          // own[] read by all before it is rewritten
+    if (!more) break;
+  }
+  for (int bb = blockIdx.x; bb < p.batch; bb += gridDim.x) {
+    if (req_tiles(ctx_eff(p.context_lens[bb], p.cap)) != 0) continue;
+    for (int j = 0; j < NEXT_N; ++j) {
+      int32_t* out = p.indices + ((int64_t)bb * NEXT_N + j) * p.idx_stride;
+      for (int i = etid; i < k; i += NT) out[i] = -1;
+    }
+  }
+}
+
+template <int NEXT_N, int H, bool FUSED>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
                  const TcParams p) {
@@ -592,6 +703,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         }
       }
     }
+    if constexpr (FUSED)
+      fused_topk<NEXT_N>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x - kFirstEpiWarp * 32, abort_flag);
   }
 
   // ---- -inf fill past each request's last tile --------------------------------
@@ -715,7 +828,7 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-template <int NEXT_N, int H>
+template <int NEXT_N, int H, bool FUSED>
 cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   using K = Cfg<NEXT_N, H>;
   EncodeTiled enc = encode_fn();
@@ -754,7 +867,8 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC);
   const size_t smem = (size_t)L.total + 1024;
   static int smem_set[64] = {0};
-  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H>, smem, smem_set);
+  static_assert(K::STAGES * kStageBytes >= (int)kSelectSmem + 1024, "fused top-k scratch fits the K ring");
+  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED>, smem, smem_set);
   if (e != cudaSuccess) return e;
 
   TcParams p;
@@ -763,6 +877,7 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   p.logits = a.logits; p.stride = a.stride; p.width = a.width;
   p.cap = min(a.width, a.bt_stride * (int64_t)P);
   p.batch = a.batch; p.status = a.status;
+  p.indices = a.indices; p.idx_stride = a.idx_stride; p.k = a.k; p.req_counter = a.req_counter;
   const int grid = device_sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
   // Programmatic dependent launch: the CTAs may be scheduled (barrier set-up,
@@ -777,7 +892,7 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H>, tkv, tq, p);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H, FUSED>, tkv, tq, p);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -785,15 +900,16 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream) {
+  const bool fused = a.indices != nullptr;
   switch (a.next_n * 1000 + a.heads) {
-    case 1064: return launch_tc<1, 64>(a, stream);
-    case 2064: return launch_tc<2, 64>(a, stream);
-    case 3064: return launch_tc<3, 64>(a, stream);
-    case 4064: return launch_tc<4, 64>(a, stream);
-    case 1128: return launch_tc<1, 128>(a, stream);
-    case 2128: return launch_tc<2, 128>(a, stream);
-    case 3128: return launch_tc<3, 128>(a, stream);
-    case 4128: return launch_tc<4, 128>(a, stream);
+    case 1064: return fused ? launch_tc<1, 64, true>(a, stream) : launch_tc<1, 64, false>(a, stream);
+    case 2064: return fused ? launch_tc<2, 64, true>(a, stream) : launch_tc<2, 64, false>(a, stream);
+    case 3064: return fused ? launch_tc<3, 64, true>(a, stream) : launch_tc<3, 64, false>(a, stream);
+    case 4064: return fused ? launch_tc<4, 64, true>(a, stream) : launch_tc<4, 64, false>(a, stream);
+    case 1128: return fused ? launch_tc<1, 128, true>(a, stream) : launch_tc<1, 128, false>(a, stream);
+    case 2128: return fused ? launch_tc<2, 128, true>(a, stream) : launch_tc<2, 128, false>(a, stream);
+    case 3128: return fused ? launch_tc<3, 128, true>(a, stream) : launch_tc<3, 128, false>(a, stream);
+    case 4128: return fused ? launch_tc<4, 128, true>(a, stream) : launch_tc<4, 128, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

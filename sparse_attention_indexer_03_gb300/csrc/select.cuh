@@ -1,0 +1,249 @@
+// Exact top-k selection of one row of fp32 logits by a group of NT threads
+// (a whole CTA, or a named-barrier group inside a larger CTA).  Used by the
+// top-k kernels and by the fused logits + top-k kernel.
+//
+// Keys are order-preserving 32-bit images of the values (-0 and +0 equal).
+// The k-th largest key is found by a radix select with digits of 8, 12 and 12
+// bits, most significant first.  Pass 1 sees every key, and real logits share
+// their top bits, so its histogram is kept per lane (256 bins x 32 lanes):
+// the lanes of one atomic never hit the same word or bank.  Passes 2 and 3
+// see only the keys of the chosen bin and use one plain 4096-bin histogram
+// each.  The select stops as soon as every key of the chosen bin is taken.
+// Output order is deterministic: the columns strictly above the threshold,
+// ascending, then the ties at the threshold, lowest columns first.
+#pragma once
+
+#include "common.cuh"
+
+namespace sai {
+
+constexpr int kSelBins1 = 256;
+constexpr int kSelBins2 = 4096;
+constexpr int kSelSpare = 32;   // one word per lane that absorbs the adds of keys outside the bin
+// Shared memory the radix select needs: its histograms and the spare words (48 KB + 128 B).
+constexpr size_t kSelectSmem = (size_t)(kSelBins1 * 32 + kSelBins2 + kSelSpare) * sizeof(uint32_t);
+
+struct SelectResult {
+  uint32_t prefix;     // digits chosen so far
+  uint32_t mask;       // bits those digits cover
+  uint32_t remaining;  // keys still to take from the chosen bin
+};
+
+template <int NT>
+struct SelectShared {
+  uint32_t wtot[NT / 32];         // per-warp totals of a pass's bins
+  uint32_t warp_gt[NT / 32];      // compaction: per-warp counts
+  uint32_t warp_eq[NT / 32];
+  uint32_t digit, remaining, bin_count;
+};
+
+// Radix select over the keys each thread visits through `for_each(f)`, which
+// calls f(valid, key) for each of the thread's keys.  Every visited key makes
+// one shared atomic add, to its bin or to the lane's spare word, so the
+// counting loops carry no data-dependent branch.  `tid` is the thread's
+// index in the group (0 .. NT-1, whole warps), `bar()` a barrier of the group,
+// `hist` kSelectSmem bytes of shared memory.  Three barriers per pass.
+template <int NT, typename Bar, typename ForEach>
+__device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint32_t* hist, uint32_t k, int tid,
+                                                     Bar bar, ForEach for_each) {
+  constexpr int kW = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* h1 = hist;                              // pass 1: [bin][lane]; pass 3: plain, reused
+  uint32_t* h2 = hist + kSelBins1 * 32;             // pass 2: plain
+  uint32_t* spare = h2 + kSelBins2 + lane;
+  for (int i = tid; i < kSelBins1 * 32 + kSelBins2; i += NT) hist[i] = 0;
+  bar();
+  SelectResult s{0u, 0u, k};
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 24 : (pass == 1 ? 12 : 0);
+    const int nb = pass == 0 ? kSelBins1 : kSelBins2;
+    uint32_t* h = pass == 1 ? h2 : h1;
+    if (pass == 1)                                  // pass 3 reuses h1, free since pass 1's search
+      for (int i = tid; i < kSelBins2; i += NT) h1[i] = 0;
+    const uint32_t prefix = s.prefix, mask = s.mask;
+    if (pass == 0) {
+      for_each([&](bool valid, uint32_t key) {
+        atomicAdd(valid ? &h1[(key >> 24) * 32 + lane] : spare, 1u);
+      });
+    } else {
+      for_each([&](bool valid, uint32_t key) {
+        const bool in = valid && (key & mask) == prefix;
+        atomicAdd(in ? &h[(key >> shift) & (uint32_t)(nb - 1)] : spare, 1u);
+      });
+    }
+    bar();
+    // Thread (warp w, lane l) owns bins w * 32 * per + 32 * i + l, i < per:
+    // a warp reads rows of 32 consecutive bins, one per bank.  Bins past nb
+    // (threads beyond the 256 bins of pass 1) count zero.
+    const int per = nb >= NT ? nb / NT : 1;
+    const int wbase = warp * 32 * per;
+    auto count = [&](int bin) -> uint32_t {
+      if (bin >= nb) return 0u;
+      if (pass != 0) return h[bin];
+      uint32_t c = 0;                               // sum of the 32 lane copies, staggered by bank
+#pragma unroll 8
+      for (int l = 0; l < 32; ++l) c += h1[bin * 32 + ((l + bin) & 31)];
+      return c;
+    };
+    constexpr int kMaxPer = kSelBins2 / NT > 1 ? kSelBins2 / NT : 1;
+    uint32_t cnt[kMaxPer];
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      cnt[i] = i < per ? count(wbase + 32 * i + lane) : 0u;
+      mine += cnt[i];
+    }
+    const uint32_t wsum = __reduce_add_sync(0xffffffffu, mine);
+    if (lane == 0) sh.wtot[warp] = wsum;
+    bar();
+    uint32_t above = 0;                             // keys in the warps above this one
+    for (int w = warp + 1; w < kW; ++w) above += sh.wtot[w];
+    const uint32_t rem = s.remaining;
+    if (above < rem && above + wsum >= rem) {       // warp-uniform: the bin is in this warp
+#pragma unroll
+      for (int i = kMaxPer - 1; i >= 0; --i) {
+        if (i < per) {
+          const uint32_t rt = __reduce_add_sync(0xffffffffu, cnt[i]);
+          if (above + rt >= rem) {                  // warp-uniform: the bin is in this row
+            uint32_t suf = cnt[i];                  // sum over lanes >= this one
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
+              if (lane + o < 32) suf += t;
+            }
+            const uint32_t ab = above + suf - cnt[i];
+            if (ab < rem && ab + cnt[i] >= rem) {
+              sh.digit = (uint32_t)(wbase + 32 * i + lane);
+              sh.remaining = rem - ab;
+              sh.bin_count = cnt[i];
+            }
+            break;
+          }
+          above += rt;
+        }
+      }
+    }
+    bar();
+    s.prefix |= sh.digit << shift;
+    s.mask |= (uint32_t)(nb - 1) << shift;
+    s.remaining = sh.remaining;
+    if (sh.bin_count == sh.remaining) break;        // every key of the chosen bin is selected
+  }
+  return s;
+}
+
+// Ordered compaction of the selection over keys key_at(i), i in [0, n): warp w
+// owns columns [w * seg, (w + 1) * seg); two sweeps (count, then write), each
+// reading kU chunks of 32 keys before using them so the reads overlap.
+template <int NT, typename Bar, typename KeyAt>
+__device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const SelectResult& s, int64_t n, int k,
+                                               int32_t* out, int tid, Bar bar, KeyAt key_at) {
+  constexpr int kW = NT / 32, kU = 4;
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t n_gt = (uint32_t)k - s.remaining;
+  const int64_t seg = ((n + kW - 1) / kW + 31) / 32 * 32;
+  const int64_t lo = warp * seg, hi = min(n, lo + seg);
+  uint32_t c_gt = 0, c_eq = 0;
+  for (int64_t base = lo; base < hi; base += 32 * kU) {
+    uint32_t m[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) m[u] = key_at(min(base + u * 32 + lane, n - 1)) & s.mask;   // n > k >= 1
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const bool v = base + u * 32 + lane < hi;
+      c_gt += (v && m[u] > s.prefix) ? 1u : 0u;
+      c_eq += (v && m[u] == s.prefix) ? 1u : 0u;
+    }
+  }
+  c_gt = __reduce_add_sync(0xffffffffu, c_gt);
+  c_eq = __reduce_add_sync(0xffffffffu, c_eq);
+  if (lane == 0) { sh.warp_gt[warp] = c_gt; sh.warp_eq[warp] = c_eq; }
+  bar();
+  uint32_t off_gt = 0, off_eq = 0;
+  for (int w = 0; w < warp; ++w) { off_gt += sh.warp_gt[w]; off_eq += sh.warp_eq[w]; }
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int64_t base = lo; base < hi; base += 32 * kU) {
+    uint32_t m[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) m[u] = key_at(min(base + u * 32 + lane, n - 1)) & s.mask;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      const bool gt = i < hi && m[u] > s.prefix, eq = i < hi && m[u] == s.prefix;
+      const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t rank = off_eq + __popc(be & lt);
+      const uint32_t pos = gt ? off_gt + __popc(bg & lt) : n_gt + rank;
+      if (gt || (eq && rank < s.remaining)) out[pos] = (int32_t)i;
+      off_gt += __popc(bg);
+      off_eq += __popc(be);
+    }
+  }
+  bar();                                            // warp_gt / warp_eq free for the next row
+}
+
+// Top-k of one row read from global memory (through L2: written by other
+// CTAs of the same launch, or by an earlier kernel).  Row length n > k.
+// Each thread reads kU keys before counting them, so the reads overlap.
+template <int NT, typename Bar>
+__device__ __forceinline__ void topk_row_stream(const float* row, int64_t n, int k, int32_t* out,
+                                                SelectShared<NT>& sh, uint32_t* hist, int tid, Bar bar) {
+  constexpr int kU = 8;
+  auto for_each = [&](auto&& f) {
+    for (int64_t base = 0; base < n; base += (int64_t)NT * kU) {
+      uint32_t key[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        key[u] = float_key(__ldcg(row + min(base + u * NT + tid, n - 1)));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) f(base + u * NT + tid < n, key[u]);
+    }
+  };
+  const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each);
+  compact_stream<NT>(sh, s, n, k, out, tid, bar, [&](int64_t i) { return float_key(__ldcg(row + i)); });
+}
+
+// Keys of row[0, n) copied into shared memory: key of column c at keys[c].
+// `keys` must have room for n + 3 words past `base`; the returned pointer is
+// `base` shifted by 0..3 words so that 16-byte row segments land on 16-byte
+// shared addresses.  No barrier: the caller's next group barrier publishes it.
+template <int NT>
+__device__ __forceinline__ uint32_t* stage_keys(const float* row, int n, uint32_t* base, int tid) {
+  const int head = min(n, (int)(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 2));
+  uint32_t* keys = base + ((4 - head) & 3);
+  if (tid < head) keys[tid] = float_key(__ldcg(row + tid));
+  const float4* v = reinterpret_cast<const float4*>(row + head);
+  uint4* kv = reinterpret_cast<uint4*>(keys + head);
+  const int nv = (n - head) >> 2;
+  constexpr int kU = 4;
+  for (int b = 0; b < nv; b += NT * kU) {
+    float4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = b + u * NT + tid;
+      if (i < nv) x[u] = __ldcg(v + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = b + u * NT + tid;
+      if (i < nv) kv[i] = make_uint4(float_key(x[u].x), float_key(x[u].y), float_key(x[u].z), float_key(x[u].w));
+    }
+  }
+  for (int i = head + nv * 4 + tid; i < n; i += NT) keys[i] = float_key(__ldcg(row + i));
+  return keys;
+}
+
+// Top-k of a row whose keys are in shared memory (stage_keys).  Row length n > k.
+template <int NT, typename Bar>
+__device__ __forceinline__ void topk_row_smem(const uint32_t* keys, int n, int k, int32_t* out,
+                                              SelectShared<NT>& sh, uint32_t* hist, int tid, Bar bar) {
+  auto for_each = [&](auto&& f) {
+#pragma unroll 4
+    for (int i = tid; i < n; i += NT) f(true, keys[i]);
+  };
+  const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each);
+  compact_stream<NT>(sh, s, n, k, out, tid, bar, [&](int64_t i) { return keys[i]; });
+}
+
+}  // namespace sai

@@ -30,6 +30,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     assert {"sai_paged_mqa_logits", "sai_top_k_per_row_decode", "sai_top_k_workspace_bytes",
+            "sai_paged_mqa_logits_topk", "sai_paged_mqa_logits_topk_workspace_bytes",
             "sai_error_string", "sai_version"} <= names
 
 
@@ -133,10 +134,45 @@ def test_topk_argument_validation(lib, kw, code):
     assert _topk(lib, **kw) == code
 
 
+def _fused(lib, **kw):
+    args = dict(q=A16, kv=A16, num_pages=20, page_size=16, weights=A16, ctx=A4, bt=A4, bt_stride=20,
+                batch=2, next_n=1, heads=64, head_dim=128, logits=A4, stride=512, W=512, k=64, idx=A4,
+                idx_stride=64, ws=A4, ws_bytes=8, status=None)
+    args.update(kw)
+    return lib.sai_paged_mqa_logits_topk(
+        args["q"], args["kv"], args["num_pages"], args["page_size"], args["weights"], args["ctx"],
+        args["bt"], args["bt_stride"], args["batch"], args["next_n"], args["heads"], args["head_dim"],
+        args["logits"], args["stride"], args["W"], args["k"], args["idx"], args["idx_stride"],
+        args["ws"], args["ws_bytes"], args["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=-1), sai.ERR_INVALID_ARGUMENT),
+    (dict(q=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(logits=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(idx=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(k=0), sai.ERR_INVALID_ARGUMENT),
+    (dict(idx_stride=63), sai.ERR_INVALID_ARGUMENT),
+    (dict(stride=511), sai.ERR_INVALID_ARGUMENT),
+    (dict(k=70000, idx_stride=70000), sai.ERR_UNSUPPORTED),
+    (dict(heads=96), sai.ERR_UNSUPPORTED),
+    (dict(q=A16 + 8), sai.ERR_MISALIGNED),
+    (dict(idx=A4 + 2), sai.ERR_MISALIGNED),
+    (dict(ws=A4 + 1), sai.ERR_MISALIGNED),
+    (dict(ws=None), sai.ERR_WORKSPACE),
+    (dict(ws_bytes=7), sai.ERR_WORKSPACE),
+    (dict(batch=0, ws_bytes=0), sai.OK),
+])
+def test_fused_argument_validation(lib, kw, code):
+    assert _fused(lib, **kw) == code
+
+
 def test_workspace_query(lib):
     n = lib.sai_top_k_workspace_bytes(1024, 32768, 2048)
     assert n >= 0
     assert lib.sai_top_k_workspace_bytes(-1, 10, 10) == 0
+    assert lib.sai_paged_mqa_logits_topk_workspace_bytes(1000) == 4000
+    assert lib.sai_paged_mqa_logits_topk_workspace_bytes(-1) == 0
 
 
 def test_binding_refuses_cpu_tensors():
