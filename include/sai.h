@@ -197,6 +197,43 @@ SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_ca
                               void* workspace, size_t workspace_bytes,
                               uint32_t* status, sai_stream_t stream);
 
+/*
+ * sai_paged_mqa_logits_topk_static -- sai_paged_mqa_logits_topk without a
+ * caller workspace.
+ *
+ * The source pages have no counterpart of this entry point.  It serves
+ * callers that cannot allocate or lend device memory: an engine whose device
+ * memory plan is fixed before it runs, a plugin interface that passes only a
+ * kernel's inputs and outputs, a C caller with no CUDA allocator at hand.  It
+ * allocates nothing either: the per-request counters live in a static device
+ * array of 16384 int32 (64 KB) inside libsai.
+ *
+ * Arguments and results are those of sai_paged_mqa_logits_topk minus the
+ * workspace.  batch > 16384 returns SAI_ERR_WORKSPACE before any CUDA call.
+ *
+ *   - Set-up: the first call with a given device current looks up the
+ *     array's device address on that device (cudaGetSymbolAddress) and keeps
+ *     it; a failure there returns SAI_ERR_CUDA.  Make that first call, on
+ *     every device used, before any stream capture begins.
+ *   - Zero state: the counters are zero when the library is loaded, and every
+ *     call that completes leaves them zero.  After a call that raised
+ *     SAI_STATUS_TIMEOUT they may hold partial counts, and later calls of
+ *     this entry point on that device may select from incomplete rows: use
+ *     sai_paged_mqa_logits_topk with a zeroed workspace from then on.
+ *   - Concurrency: all calls on one device share the counters.  Two calls in
+ *     flight at once (on different streams, or from different threads
+ *     without ordering) race on them and give wrong indices; order such calls
+ *     on one stream.
+ */
+SAI_API int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t* kv_cache,
+                              int64_t num_pages, int32_t page_size,
+                              const float* weights, const int32_t* context_lens,
+                              const int32_t* block_table, int64_t block_table_stride,
+                              int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim,
+                              float* logits, int64_t logits_stride, int64_t max_model_len,
+                              int32_t k, int32_t* indices, int64_t indices_stride,
+                              uint32_t* status, sai_stream_t stream);
+
 /* Static, human-readable name of a return code. */
 SAI_API const char* sai_error_string(int code);
 

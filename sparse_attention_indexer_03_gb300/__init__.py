@@ -23,7 +23,7 @@ from . import _build
 __all__ = [
     "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
     "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
-    "logits_topk_workspace_bytes", "paged_mqa_logits_topk",
+    "logits_topk_workspace_bytes", "paged_mqa_logits_topk", "paged_mqa_logits_topk_static",
     "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
     "KV_PAGE_SPLIT", "KV_INTERLEAVED",
 ]
@@ -71,6 +71,10 @@ _SIGS = {
                                              _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                              _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _c.c_int64,
                                              _P, _c.c_size_t, _P, _P]),
+    "sai_paged_mqa_logits_topk_static": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int32, _P, _P, _P, _c.c_int64,
+                                                    _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                                    _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _c.c_int64,
+                                                    _P, _P]),
     "sai_error_string": (_c.c_char_p, [_c.c_int]),
     "sai_version": (_c.c_int, []),
 }
@@ -211,6 +215,25 @@ def paged_mqa_logits_topk(q, kv_cache, page_size: int, weights, context_lens, bl
         _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_paged_mqa_logits_topk")
+
+
+def paged_mqa_logits_topk_static(q, kv_cache, page_size: int, weights, context_lens, block_table,
+                                 logits, max_model_len: int, k: int, indices, *,
+                                 num_pages: Optional[int] = None, status=None, stream=None) -> None:
+    """`paged_mqa_logits_topk` with the library's static counters instead of a
+    workspace (see `sai_paged_mqa_logits_topk_static`: batch <= 16384, calls
+    on one device must not overlap)."""
+    import torch
+
+    if indices.dim() != 2 or indices.stride(1) != 1:
+        raise ValueError("indices must be [rows, stride] with unit inner stride")
+    args = _logits_args(q, kv_cache, page_size, weights, context_lens, block_table, logits,
+                        max_model_len, num_pages)
+    code = library().sai_paged_mqa_logits_topk_static(
+        *args, int(k), _ptr(indices, torch.int32, "indices"), int(indices.stride(0)),
+        _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_paged_mqa_logits_topk_static")
 
 
 def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:

@@ -3,6 +3,7 @@
 // nor any output.
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -82,6 +83,31 @@ int check_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_page
   return SAI_OK;
 }
 
+// Request counters of sai_paged_mqa_logits_topk_static, for callers that
+// cannot hand the library any memory of their own.  Zero when the module is
+// loaded; every call that completes leaves them zero again.
+constexpr int kStaticMaxBatch = 16384;
+static __device__ __align__(256) int32_t g_static_counters[kStaticMaxBatch];
+
+std::mutex g_static_mu;
+int32_t* g_static_ptr[64] = {};
+
+// Device address of this device's counters, looked up once per device (on
+// the first call made with that device current).
+int static_counters(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SAI_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SAI_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_counters) != cudaSuccess || p == nullptr) return SAI_ERR_CUDA;
+    g_static_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return SAI_OK;
+}
+
 }  // namespace
 }  // namespace sai
 
@@ -129,6 +155,32 @@ int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache, int
   if (batch == 0) return SAI_OK;
   a.indices = indices; a.idx_stride = indices_stride; a.k = k;
   a.req_counter = static_cast<int32_t*>(workspace);
+  return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages,
+                                     int32_t page_size, const float* weights, const int32_t* context_lens,
+                                     const int32_t* block_table, int64_t block_table_stride, int32_t batch,
+                                     int32_t next_n, int32_t heads, int32_t head_dim, float* logits,
+                                     int64_t logits_stride, int64_t max_model_len, int32_t k, int32_t* indices,
+                                     int64_t indices_stride, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  LogitsArgs a;
+  const int rc = check_logits(q_fp8, kv_cache, num_pages, page_size, weights, context_lens, block_table,
+                              block_table_stride, batch, next_n, heads, head_dim, logits, logits_stride,
+                              max_model_len, SAI_KV_PAGE_SPLIT, status, a);
+  if (rc != SAI_OK) return rc;
+  if (k < 1 || indices_stride < k || !indices) return SAI_ERR_INVALID_ARGUMENT;
+  if (k > 65536 || max_model_len > INT32_MAX) return SAI_ERR_UNSUPPORTED;
+  if (indices_stride > (INT64_MAX / 8) / ((int64_t)batch * next_n + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if (!aligned(indices, 4)) return SAI_ERR_MISALIGNED;
+  if (batch > kStaticMaxBatch) return SAI_ERR_WORKSPACE;
+  if (batch == 0) return SAI_OK;
+  int32_t* counters = nullptr;
+  const int sc = static_counters(&counters);
+  if (sc != SAI_OK) return sc;
+  a.indices = indices; a.idx_stride = indices_stride; a.k = k;
+  a.req_counter = counters;
   return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
