@@ -85,6 +85,10 @@ struct TcParams {
   int32_t* req_counter;   // [batch] tiles counted in so far, zero between launches
 };
 
+// Batches up to this many requests have their context lengths copied into
+// shared memory by the partition, so the walks over requests read them there.
+constexpr int kCtxSmem = 512;
+
 template <int NEXT_N, int H>
 struct Cfg {
   static constexpr int N = NEXT_N * H;
@@ -97,7 +101,8 @@ struct Cfg {
   static constexpr int Q_BYTES = N * kHeadDim;
   static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(kTile, NC);
   // K ring depth: as many 128-token stages as fit beside two Q slots (at most 8).
-  static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64;
+  static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64 +
+                               kCtxSmem * 4;
   static constexpr int PER_STAGE = kStageBytes + kScaleSlot + 16 + 16;
   static constexpr int STAGES = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
   static_assert(STAGES >= 2, "shared memory");
@@ -110,7 +115,7 @@ struct Part {        // this CTA's share of the work
 };
 
 struct SmemLayout {
-  uint32_t k, q, sc, meta, ids, bar, misc, total;
+  uint32_t k, q, sc, meta, ids, bar, misc, ctx, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc) {
@@ -122,7 +127,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int a
   L.ids = L.meta + stages * 16;
   L.bar = L.ids + kProducers * kLookahead * 32 * 4;
   L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1);
-  L.total = L.misc + 64;
+  L.ctx = L.misc + 64;
+  L.total = L.ctx + kCtxSmem * 4;
   return L;
 }
 
@@ -165,11 +171,12 @@ __device__ __forceinline__ int64_t split_begin(int64_t n, int64_t g, int64_t i) 
 constexpr int kCtxRegs = 16;
 
 template <int NEXT_N>
-__device__ void compute_partition(const TcParams& p, Part* part, int lane) {
+__device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s, int lane) {
   const int64_t G = gridDim.x, cta = blockIdx.x;
   int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
   int64_t tb = 0, te = 0, ub = 0, ue = 0;
   bool clamped = false;
+  static_assert(32 * kCtxRegs == kCtxSmem, "every request of a staged batch is read by the register path");
   if (p.batch <= 32 * kCtxRegs) {
     const int R = (p.batch + 31) / 32;
     int32_t tl[kCtxRegs], ul[kCtxRegs];
@@ -179,6 +186,7 @@ __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
       const int b = lane * R + x;
       const bool v = x < R && b < p.batch;
       const int64_t raw = v ? (int64_t)p.context_lens[b] : 0;
+      if (v) ctx_s[b] = (int32_t)raw;
       clamped |= v && (raw < 0 || raw > p.cap);
       const int64_t ce = ctx_eff(raw, p.cap);
       tl[x] = (int32_t)req_tiles(ce);
@@ -249,15 +257,34 @@ __device__ void compute_partition(const TcParams& p, Part* part, int lane) {
   }
 }
 
+// L2 prefetch of the block-table entries the launch may read (each row's
+// first min(stride, ceil(cap / P)) entries), split evenly over the CTAs: run
+// while the partition reads the context lengths, it turns the producers'
+// first page-id reads into L2 hits.  A prefetch only loads lines into L2, so
+// it may run before the previous kernel in the stream has completed.
+__device__ void prefetch_block_table(const TcParams& p, int lane) {
+  const int64_t used = min(p.bt_stride, (p.cap + p.page_size - 1) / p.page_size);
+  const int64_t lines_per_row = (used * 4 + 127) / 128 + 1;      // + 1: a row need not start on a line
+  const int64_t total = (int64_t)p.batch * lines_per_row;
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t x0 = (int64_t)blockIdx.x * per, x1 = min(total, x0 + per);
+  for (int64_t x = x0 + lane; x < x1; x += 32) {
+    const int64_t r = x / lines_per_row, l = x - r * lines_per_row;
+    const char* row = reinterpret_cast<const char*>(p.block_table + r * p.bt_stride);
+    if (l * 128 < used * 4) ptx::prefetch_l2(row + l * 128);
+  }
+}
+
 // Context lengths of requests [base, base + 32) held one per lane, so a warp
 // walking requests in order reads them from registers.
 struct CtxCache {
+  const int32_t* staged = nullptr;                 // shared-memory copy, if the batch has one
   int base = -1000000;
   int64_t mine = 0;
   __device__ __forceinline__ int64_t get(const TcParams& p, int b, int lane) {
     if (b < base || b >= base + 32) {              // warp-uniform
       base = b;
-      mine = (b + lane < p.batch) ? (int64_t)p.context_lens[b + lane] : 0;
+      mine = (b + lane < p.batch) ? (int64_t)(staged ? staged[b + lane] : p.context_lens[b + lane]) : 0;
     }
     return __shfl_sync(0xffffffffu, mine, b - base);
   }
@@ -297,13 +324,14 @@ struct Cursor {
 // whose addition completes the request's tile count resets the counter to 0
 // and runs the top-k of the request's rows, reading them through L2.  No CTA
 // ever waits for another.  Requests without tiles get their -1 rows from CTA
-// (b mod grid).  Runs on the two epilogue warpgroups (256 threads, named
-// barrier 1); the drained K-stage ring holds the selection's histograms.
-constexpr int kFusedThreads = kEpiWarps * 32;
+// (b mod grid).  Runs on all warps of the CTA once its roles and its share of
+// the -inf fill are done (named barrier 1); the drained K-stage ring holds the
+// selection's histograms.
+constexpr int kFusedThreads = kThreadsTc;
 constexpr int kOwnMax = 64;
 
-struct EpiBar {
-  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+struct TailBar {
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 384;" ::: "memory"); }
 };
 
 // `ring` is the drained part of shared memory (K stages and Q slots, `ring_bytes`
@@ -311,10 +339,11 @@ struct EpiBar {
 // select, then the keys of rows that fit (longer rows are re-read from L2).
 template <int NEXT_N>
 __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int ring_bytes, int etid,
-                           const volatile int* abort_flag) {
+                           const int32_t* staged, const volatile int* abort_flag) {
+  auto ctx_of = [&](int b) -> int64_t { return staged ? staged[b] : p.context_lens[b]; };
   constexpr int NT = kFusedThreads;
-  static_assert(NT == 256, "named barrier 1 counts 256 threads");
-  const EpiBar ebar;
+  static_assert(NT == 384, "named barrier 1 counts 384 threads");
+  const TailBar ebar;
   uint32_t* hist = reinterpret_cast<uint32_t*>(ring);
   auto* sh = reinterpret_cast<SelectShared<NT>*>(ring + kSelectSmem);
   int* own = reinterpret_cast<int*>(ring + kSelectSmem + 512);   // [0] count (-1: stop), [1] more, [2..] requests
@@ -334,7 +363,7 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
       const bool stop = *abort_flag != 0;
       while (!stop && left > 0 && n_own + 32 <= kOwnMax) {
         const int bb = b + lane;
-        const int64_t nt = bb < p.batch ? req_tiles(ctx_eff(p.context_lens[bb], p.cap)) : 0;
+        const int64_t nt = bb < p.batch ? req_tiles(ctx_eff(ctx_of(bb), p.cap)) : 0;
         const int64_t avail = lane == 0 ? nt - t : nt;
         const int64_t incl = warp_incl_scan64(avail, lane);
         const int64_t m = min(avail, max((int64_t)0, (int64_t)left - (incl - avail)));
@@ -367,7 +396,7 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
     if (n_own < 0) return;                           // a wait timed out: leave the rest
     for (int o = 0; o < n_own; ++o) {
       const int bb = own[2 + o];
-      const int64_t raw = p.context_lens[bb];
+      const int64_t raw = ctx_of(bb);
 #pragma unroll 1
       for (int j = 0; j < NEXT_N; ++j) {
         const int64_t r = (int64_t)bb * NEXT_N + j;
@@ -388,7 +417,7 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
     if (!more) break;
   }
   for (int bb = blockIdx.x; bb < p.batch; bb += gridDim.x) {
-    if (req_tiles(ctx_eff(p.context_lens[bb], p.cap)) != 0) continue;
+    if (req_tiles(ctx_eff(ctx_of(bb), p.cap)) != 0) continue;
     for (int j = 0; j < NEXT_N; ++j) {
       int32_t* out = p.indices + ((int64_t)bb * NEXT_N + j) * p.idx_stride;
       for (int i = etid; i < k; i += NT) out[i] = -1;
@@ -421,7 +450,10 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   int* fill_next = reinterpret_cast<int*>(smem + L.misc + 8);      // next -inf fill unit to take
+  volatile int* epi_done = reinterpret_cast<volatile int*>(smem + L.misc + 12);   // epilogue warps finished
   Part* part = reinterpret_cast<Part*>(smem + L.misc + 16);
+  int32_t* ctx_s = reinterpret_cast<int32_t*>(smem + L.ctx);
+  const int32_t* staged = p.batch <= kCtxSmem ? ctx_s : nullptr;   // written by the partition
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -434,7 +466,9 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     // Inputs may come from the previous kernel in the stream, and the logits
     // buffer may still be read by it: wait for it before touching either.
     ptx::wait_prerequisites();
-    compute_partition<NEXT_N>(p, part, lane);
+    compute_partition<NEXT_N>(p, part, ctx_s, lane);
+  } else if (warp == 1) {
+    prefetch_block_table(p, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
@@ -452,6 +486,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       ptx::mbar_init(drain, 1);
       *abort_flag = 0;
       *fill_next = 0;
+      *epi_done = 0;
       ptx::fence_barrier_init();
     }
     __syncwarp();
@@ -495,6 +530,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     // request starts (its own tiles' and the other warps'): waiting on a Q
     // slot's release in sequence keeps each parity wait unambiguous.
     CtxCache cc, cc_la;
+    cc.staged = cc_la.staged = staged;
     Cursor cur, la;
     int q_seq = 0, ci = 0;                               // ci: tile index of `cur`
     bool qok = true;
@@ -540,7 +576,9 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
       ptx::cp_async_commit();
     };
-    for (int k = 0; k < kLookahead; ++k) issue_ids();
+    // Only the first tile's page ids go out before its K copies; the rest of
+    // the lookahead follows them, off the first tile's latency chain.
+    issue_ids();
     bool ok = true;
     int j = 0;
     for (; j < own && ok; ++j) {
@@ -552,7 +590,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const int qs = q_seq & 1;
       if (!qok) { ok = false; break; }
       if (!ptx::mbar_wait_warp(kempty(s), ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
-      ptx::cp_async_wait<kLookahead - 1>();                  // page ids of this tile have landed
+      if (j == 0) ptx::cp_async_wait<0>();                    // page ids of this tile have landed
+      else ptx::cp_async_wait<kLookahead - 1>();
       const int64_t tok0 = (int64_t)cur.t * kTile + (P >= kTile ? 0 : (int64_t)pl * P);
       const bool need = pl < ppt && tok0 < cur.ce;
       const int64_t pg = (int64_t)ring_ptr[(j % kLookahead) * 32 + pl];   // widened before use
@@ -580,6 +619,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         ptx::bulk_load(sdst, src, (uint32_t)tok_per_box * kScaleBytes, full(s), pol_k);
       }
       __syncwarp();
+      if (j == 0)
+        for (int k = 1; k < kLookahead; ++k) issue_ids();     // the lookahead, after the first copies
       issue_ids();                                             // refill the slot just read
       if (j + 1 < own)
         for (int x = 0; x < kProducers; ++x) step();
@@ -669,7 +710,9 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
 #pragma unroll
       for (int jr = 0; jr < K::ROWS; ++jr) {
         const float4* wrow = w0 + jr * (H / 4);
-        float accum = 0.f;
+        // Eight independent partial sums: one dependent chain of H fused
+        // multiply-adds would bound the epilogue by FMA latency.
+        float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h0 = 0; h0 < H; h0 += 64) {         // two 32-column TMEM loads, one wait
           uint32_t v[64];
@@ -681,13 +724,14 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            accum = fmaf(w4[x].x, fmaxf(__uint_as_float(v[4 * x + 0]), 0.f), accum);
-            accum = fmaf(w4[x].y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), accum);
-            accum = fmaf(w4[x].z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), accum);
-            accum = fmaf(w4[x].w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), accum);
+            float* q4 = part + 4 * (x & 1);
+            q4[0] = fmaf(w4[x].x, fmaxf(__uint_as_float(v[4 * x + 0]), 0.f), q4[0]);
+            q4[1] = fmaf(w4[x].y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), q4[1]);
+            q4[2] = fmaf(w4[x].z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), q4[2]);
+            q4[3] = fmaf(w4[x].w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), q4[3]);
           }
         }
-        out[jr] = accum;
+        out[jr] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -703,21 +747,27 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         }
       }
     }
-    if constexpr (FUSED)
-      fused_topk<NEXT_N>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x - kFirstEpiWarp * 32, abort_flag);
+    if constexpr (FUSED) {
+      __syncwarp();
+      if (lane == 0) atomicAdd(const_cast<int*>(epi_done), 1);
+    }
   }
 
   // ---- -inf fill past each request's last tile --------------------------------
   // Every warp takes units from a shared counter once its role is done, so the
-  // warps that finish first (the producers) do most of it.
-  {
+  // warps that finish first (the producers) do most of it.  With the fused
+  // top-k, the other warps stop taking units as soon as the epilogue is done,
+  // join the selection, and all warps finish the fill after it.
+  auto run_fill = [&](bool yield_to_tail) {
     CtxCache cc;
+    cc.staged = staged;
     int b = pt.fb0;
     int64_t u_in = pt.fu0, ucur = 0;
     int64_t ce = pt.n_units > 0 ? ctx_eff(cc.get(p, b, lane), p.cap) : 0;
     int64_t fs = min(p.width, req_tiles(ce) * kTile);
     int64_t chunks = (p.width - fs + kFillCols - 1) / kFillCols;
     for (;;) {
+      if (yield_to_tail && *epi_done == kEpiWarps) break;   // warp-uniform: one shared word
       int u = 0;
       if (lane == 0) u = atomicAdd(fill_next, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
@@ -748,6 +798,13 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const int64_t tail0 = v0 + nv * 4;
       if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
     }
+  };
+  if constexpr (FUSED) {
+    if (warp < kFirstEpiWarp) run_fill(true);
+    fused_topk<NEXT_N>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x, staged, abort_flag);
+    run_fill(false);
+  } else {
+    run_fill(false);
   }
 
   // ---- tear-down ----------------------------------------------------------------
@@ -867,7 +924,8 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC);
   const size_t smem = (size_t)L.total + 1024;
   static int smem_set[64] = {0};
-  static_assert(K::STAGES * kStageBytes >= (int)kSelectSmem + 1024, "fused top-k scratch fits the K ring");
+  static_assert(K::STAGES * kStageBytes + 2 * K::Q_BYTES >= (int)kSelectSmem + 1024 + 4 * 8192,
+                "fused top-k scratch (and the keys of 8192-column rows) fit the drained K stages and Q slots");
   cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED>, smem, smem_set);
   if (e != cudaSuccess) return e;
 

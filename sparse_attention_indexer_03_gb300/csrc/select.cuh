@@ -19,9 +19,17 @@ namespace sai {
 
 constexpr int kSelBins1 = 256;
 constexpr int kSelBins2 = 4096;
-constexpr int kSelSpare = 32;   // one word per lane that absorbs the adds of keys outside the bin
-// Shared memory the radix select needs: its histograms and the spare words (48 KB + 128 B).
-constexpr size_t kSelectSmem = (size_t)(kSelBins1 * 32 + kSelBins2 + kSelSpare) * sizeof(uint32_t);
+// Shared memory the radix select needs for its histograms (48 KB).
+constexpr size_t kSelectSmem = (size_t)(kSelBins1 * 32 + kSelBins2) * sizeof(uint32_t);
+
+// Shared-memory add of 1 under a predicate, as one predicated instruction:
+// lanes whose key is outside the bin issue nothing and no branch is formed.
+__device__ __forceinline__ void count_if(uint32_t* word, bool pred) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(word);
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p red.shared.add.u32 [%0], 1;\n\t}"
+      :: "r"(a), "r"((uint32_t)pred) : "memory");
+}
 
 struct SelectResult {
   uint32_t prefix;     // digits chosen so far
@@ -38,9 +46,9 @@ struct SelectShared {
 };
 
 // Radix select over the keys each thread visits through `for_each(f)`, which
-// calls f(valid, key) for each of the thread's keys.  Every visited key makes
-// one shared atomic add, to its bin or to the lane's spare word, so the
-// counting loops carry no data-dependent branch.  `tid` is the thread's
+// calls f(valid, key) for each of the thread's keys.  The counting adds are
+// predicated instructions, so the loops carry no data-dependent branch.
+// `tid` is the thread's
 // index in the group (0 .. NT-1, whole warps), `bar()` a barrier of the group,
 // `hist` kSelectSmem bytes of shared memory.  Three barriers per pass.
 template <int NT, typename Bar, typename ForEach>
@@ -50,7 +58,6 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* h1 = hist;                              // pass 1: [bin][lane]; pass 3: plain, reused
   uint32_t* h2 = hist + kSelBins1 * 32;             // pass 2: plain
-  uint32_t* spare = h2 + kSelBins2 + lane;
   for (int i = tid; i < kSelBins1 * 32 + kSelBins2; i += NT) hist[i] = 0;
   bar();
   SelectResult s{0u, 0u, k};
@@ -63,20 +70,17 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
       for (int i = tid; i < kSelBins2; i += NT) h1[i] = 0;
     const uint32_t prefix = s.prefix, mask = s.mask;
     if (pass == 0) {
-      for_each([&](bool valid, uint32_t key) {
-        atomicAdd(valid ? &h1[(key >> 24) * 32 + lane] : spare, 1u);
-      });
+      for_each([&](bool valid, uint32_t key) { count_if(&h1[(key >> 24) * 32 + lane], valid); });
     } else {
       for_each([&](bool valid, uint32_t key) {
-        const bool in = valid && (key & mask) == prefix;
-        atomicAdd(in ? &h[(key >> shift) & (uint32_t)(nb - 1)] : spare, 1u);
+        count_if(&h[(key >> shift) & (uint32_t)(nb - 1)], valid && (key & mask) == prefix);
       });
     }
     bar();
     // Thread (warp w, lane l) owns bins w * 32 * per + 32 * i + l, i < per:
     // a warp reads rows of 32 consecutive bins, one per bank.  Bins past nb
-    // (threads beyond the 256 bins of pass 1) count zero.
-    const int per = nb >= NT ? nb / NT : 1;
+    // count zero.
+    const int per = (nb + NT - 1) / NT;
     const int wbase = warp * 32 * per;
     auto count = [&](int bin) -> uint32_t {
       if (bin >= nb) return 0u;
@@ -86,7 +90,7 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
       for (int l = 0; l < 32; ++l) c += h1[bin * 32 + ((l + bin) & 31)];
       return c;
     };
-    constexpr int kMaxPer = kSelBins2 / NT > 1 ? kSelBins2 / NT : 1;
+    constexpr int kMaxPer = (kSelBins2 + NT - 1) / NT;
     uint32_t cnt[kMaxPer];
     uint32_t mine = 0;
 #pragma unroll
@@ -180,6 +184,49 @@ __device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const Selec
     }
   }
   bar();                                            // warp_gt / warp_eq free for the next row
+}
+
+// Ordered compaction of keys held in registers, warp-contiguous: lane l of
+// warp w holds column col0 + 32 * i + l in key[i] (col0 = w * 32 * KPT), for
+// slots i < live (warp-uniform).  Per-warp counts from registers, one barrier,
+// then the write sweep.
+template <int NT, int KPT, typename Bar>
+__device__ __forceinline__ void compact_regs(SelectShared<NT>& sh, const SelectResult& s, int n, int k,
+                                             int32_t* out, int tid, Bar bar, const uint32_t (&key)[KPT],
+                                             int col0, int live) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t n_gt = (uint32_t)k - s.remaining;
+  uint32_t c_gt = 0, c_eq = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (i < live) {
+      const bool v = col0 + 32 * i + lane < n;
+      const uint32_t m = key[i] & s.mask;
+      c_gt += (v && m > s.prefix) ? 1u : 0u;
+      c_eq += (v && m == s.prefix) ? 1u : 0u;
+    }
+  }
+  c_gt = __reduce_add_sync(0xffffffffu, c_gt);
+  c_eq = __reduce_add_sync(0xffffffffu, c_eq);
+  if (lane == 0) { sh.warp_gt[warp] = c_gt; sh.warp_eq[warp] = c_eq; }
+  bar();
+  uint32_t off_gt = 0, off_eq = 0;
+  for (int w = 0; w < warp; ++w) { off_gt += sh.warp_gt[w]; off_eq += sh.warp_eq[w]; }
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (i < live) {
+      const int c = col0 + 32 * i + lane;
+      const uint32_t m = key[i] & s.mask;
+      const bool gt = c < n && m > s.prefix, eq = c < n && m == s.prefix;
+      const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t rank = off_eq + __popc(be & lt);
+      const uint32_t pos = gt ? off_gt + __popc(bg & lt) : n_gt + rank;
+      if (gt || (eq && rank < s.remaining)) out[pos] = c;
+      off_gt += __popc(bg);
+      off_eq += __popc(be);
+    }
+  }
 }
 
 // Top-k of one row read from global memory (through L2: written by other
