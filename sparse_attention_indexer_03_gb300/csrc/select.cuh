@@ -186,48 +186,77 @@ __device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const Selec
   bar();                                            // warp_gt / warp_eq free for the next row
 }
 
-// Ordered compaction of keys held in registers, warp-contiguous: lane l of
-// warp w holds column col0 + 32 * i + l in key[i] (col0 = w * 32 * KPT), for
-// slots i < live (warp-uniform).  Per-warp counts from registers, one barrier,
-// then the write sweep.
-template <int NT, int KPT, typename Bar>
-__device__ __forceinline__ void compact_regs(SelectShared<NT>& sh, const SelectResult& s, int n, int k,
-                                             int32_t* out, int tid, Bar bar, const uint32_t (&key)[KPT],
-                                             int col0, int live) {
+// Ordered compaction by lanes.  Lane l of warp w owns the run of columns
+// [base, base + len) with base = w * 32 * len + l * len, so column order is
+// (warp, lane, slot): each lane counts its own selected keys, one packed
+// warp scan gives every lane its offset, one barrier gives every warp its
+// offset, and each lane then writes its keys in order with no warp-wide
+// operation per key.  `key_at.for_each(f)` calls f(i, key) for the keys of
+// columns base + i; only i < len and columns below n count.
+template <int NT, typename Bar, typename KeyAt>
+__device__ __forceinline__ void compact_lanes(SelectShared<NT>& sh, const SelectResult& s, int n, int k,
+                                              int32_t* out, int tid, Bar bar, int base, int len, KeyAt key_at) {
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t n_gt = (uint32_t)k - s.remaining;
-  uint32_t c_gt = 0, c_eq = 0;
+  uint32_t cg = 0, ce = 0;
+  key_at.for_each([&](int i, uint32_t key) {
+    const uint32_t m = key & s.mask;
+    const bool v = i < len && base + i < n;
+    cg += (v && m > s.prefix) ? 1u : 0u;
+    ce += (v && m == s.prefix) ? 1u : 0u;
+  });
+  // Counts below 2^16 per warp (a warp owns at most 32 * len <= 65535 columns
+  // for every caller), so both scans share one word.
+  const uint32_t x = (cg << 16) | ce;
+  uint32_t incl = x;
 #pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    if (i < live) {
-      const bool v = col0 + 32 * i + lane < n;
-      const uint32_t m = key[i] & s.mask;
-      c_gt += (v && m > s.prefix) ? 1u : 0u;
-      c_eq += (v && m == s.prefix) ? 1u : 0u;
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
-  c_gt = __reduce_add_sync(0xffffffffu, c_gt);
-  c_eq = __reduce_add_sync(0xffffffffu, c_eq);
-  if (lane == 0) { sh.warp_gt[warp] = c_gt; sh.warp_eq[warp] = c_eq; }
+  if (lane == 31) { sh.warp_gt[warp] = incl >> 16; sh.warp_eq[warp] = incl & 0xffffu; }
   bar();
-  uint32_t off_gt = 0, off_eq = 0;
-  for (int w = 0; w < warp; ++w) { off_gt += sh.warp_gt[w]; off_eq += sh.warp_eq[w]; }
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    if (i < live) {
-      const int c = col0 + 32 * i + lane;
-      const uint32_t m = key[i] & s.mask;
-      const bool gt = c < n && m > s.prefix, eq = c < n && m == s.prefix;
-      const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-      const uint32_t rank = off_eq + __popc(be & lt);
-      const uint32_t pos = gt ? off_gt + __popc(bg & lt) : n_gt + rank;
-      if (gt || (eq && rank < s.remaining)) out[pos] = c;
-      off_gt += __popc(bg);
-      off_eq += __popc(be);
-    }
-  }
+  const uint32_t excl = incl - x;
+  uint32_t pg = excl >> 16, pe = excl & 0xffffu;
+  for (int w = 0; w < warp; ++w) { pg += sh.warp_gt[w]; pe += sh.warp_eq[w]; }
+  key_at.for_each([&](int i, uint32_t key) {
+    const uint32_t m = key & s.mask;
+    const int c = base + i;
+    const bool v = i < len && c < n;
+    const bool gt = v && m > s.prefix, eq = v && m == s.prefix;
+    if (gt) out[pg] = c;
+    if (eq && pe < s.remaining) out[n_gt + pe] = c;
+    pg += gt ? 1u : 0u;
+    pe += eq ? 1u : 0u;
+  });
+  bar();                                            // warp_gt / warp_eq free for the next row
 }
+
+// Keys of a lane's run held in registers: key[i], i < len <= KPT (len
+// uniform across the group, so the slot test is a uniform branch).
+template <int KPT>
+struct RegRun {
+  const uint32_t (&key)[KPT];
+  int len;
+  template <typename F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+      if (i < len) f(i, key[i]);
+  }
+};
+
+// Keys of a lane's run in shared memory: keys[base + i], i < len, read at
+// min(base + i, n - 1) so the reads stay inside the n staged keys.
+struct SmemRun {
+  const uint32_t* keys;
+  int base, len, n;
+  template <typename F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+#pragma unroll 4
+    for (int i = 0; i < len; ++i) f(i, keys[min(base + i, n - 1)]);
+  }
+};
 
 // Top-k of one row read from global memory (through L2: written by other
 // CTAs of the same launch, or by an earlier kernel).  Row length n > k.
@@ -281,16 +310,18 @@ __device__ __forceinline__ uint32_t* stage_keys(const float* row, int n, uint32_
   return keys;
 }
 
-// Top-k of a row whose keys are in shared memory (stage_keys).  Row length n > k.
+// Top-k of a row whose keys are in shared memory (stage_keys).  Row length
+// n > k.  Each lane owns a run of len consecutive columns, len odd so that
+// the 32 lanes of a warp read 32 different banks.
 template <int NT, typename Bar>
 __device__ __forceinline__ void topk_row_smem(const uint32_t* keys, int n, int k, int32_t* out,
                                               SelectShared<NT>& sh, uint32_t* hist, int tid, Bar bar) {
-  auto for_each = [&](auto&& f) {
-#pragma unroll 4
-    for (int i = tid; i < n; i += NT) f(true, keys[i]);
-  };
+  const int len = ((n + NT - 1) / NT) | 1;
+  const int base = (tid >> 5) * 32 * len + (tid & 31) * len;
+  const SmemRun run{keys, base, len, n};
+  auto for_each = [&](auto&& f) { run.for_each([&](int i, uint32_t key) { f(base + i < n, key); }); };
   const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each);
-  compact_stream<NT>(sh, s, n, k, out, tid, bar, [&](int64_t i) { return keys[i]; });
+  compact_lanes<NT>(sh, s, n, k, out, tid, bar, base, len, run);
 }
 
 }  // namespace sai
