@@ -17,12 +17,16 @@ result for comparison):
   FP8 cache through the block table.
 * `top_k_per_row`: the indices of the k largest logits of each row's valid
   columns, ties broken towards the lower index, padded with -1.
+* `kcache.quantize_k_rows` / `kcache.insert_k_rows`: the K-cache write that
+  precedes the path: per-token FP8 quantisation (scale = amax / 448) and
+  insertion into the paged cache through int64 slots.
 
 Parity status: every function here is pinned by `tests/test_oracle_*.py`
 against facts fixed outside this code (a library FP8 conversion, exact
 rational brute force, closed forms, invariants, a library sort, the byte
 values printed for the reproducer).  No function is "parity unpinned".
 """
+from . import kcache  # noqa: F401
 from .indexer import (  # noqa: F401
     E4M3FN_NAN_CODES,
     e4m3fn_table,
