@@ -450,6 +450,123 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return 0
 
 
+# ------------------------------------------------------------------ K-cache write
+KC_METRIC = "K-cache FP8 quantise + insert GB/s (bf16 K rows -> paged e4m3 cache), 1 GB300"
+KC_TOKENS, KC_PAGE, KC_PAGES = 16384, 64, 8192      # a 16384-token batch into the decode pool
+
+
+def kcache_bytes(T: int) -> int:
+    """Algorithmic HBM bytes: bf16 rows and int64 slots read, 132 bytes written per token."""
+    return T * (2 * 128 + 8 + 132)
+
+
+def run_kcache(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import sparse_attention_indexer_03_gb300 as sai
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    sai.build()
+    dev = torch.device("cuda", local_rank)
+    T, P, NP = KC_TOKENS, KC_PAGE, KC_PAGES
+    per_set = T * (2 * 128 + 8)
+    R = max(2, min(64, math.ceil(2.0 * L2_BYTES / per_set)))
+    sets = []
+    for i in range(R):
+        bits, slots = synth.kcache_batch(T, P, NP, seed=100 + i)
+        sets.append((torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev),
+                     torch.from_numpy(slots).to(dev)))
+    cache = torch.zeros(NP * P * 132, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        k, s = sets[i % R]
+        sai.indexer_k_quant_insert(k, s, cache, P, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    S = K if K <= 200 else 100
+    K = S * math.ceil(K / S)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(S):
+            step(i)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(K // S):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    ms, _ = aggregate(ms, T, world, dev)
+    assert int(status.item()) == 0
+
+    # End to end: pinned host rows and slots in, the status word out.
+    hk = torch.from_numpy(synth.kcache_batch(T, P, NP, seed=99)[0].view(np.int16)).pin_memory()
+    hs = torch.from_numpy(synth.kcache_batch(T, P, NP, seed=99)[1]).pin_memory()
+    hst = torch.zeros(1, dtype=torch.int32).pin_memory()
+    dk, ds = sets[0]
+    Ke = min(args.steps, 200)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(Ke + 3):
+            if i == 3:
+                e0.record(stream)
+            dk.view(torch.int16).copy_(hk, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            sai.indexer_k_quant_insert(dk, ds, cache, P, status=status, stream=stream)
+            hst.copy_(status, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms, _ = aggregate(e0.elapsed_time(e1), T, world, dev)
+    if rank != 0:
+        return 0
+    peaks = load_peaks()
+    nbytes = kcache_bytes(T)
+    gbs = nbytes * world * K / (ms * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        bits, slots = synth.kcache_batch(2048, P, NP, seed=7)
+        c0 = time.perf_counter()
+        reps = 0
+        small = np.zeros(NP * P * 132, np.uint8)
+        while time.perf_counter() - c0 < 5.0:
+            codes, scales = oracle.kcache.quantize_k_rows(bits)
+            oracle.kcache.insert_k_rows(small, slots, codes, scales, NP, P)
+            reps += 1
+        csec = time.perf_counter() - c0
+        cpu = {"value": kcache_bytes(2048) * reps / csec / 1e9, "unit": "GB/s", "cores": cpu_threads(),
+               "kind": "oracle", "sample": f"{reps} x 2048 tokens quantised and inserted, {csec:.1f} s"}
+    line = {"metric": KC_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
+            "config": {"workload": f"kcache: T={T} bf16 rows, P={P}, pool {NP} pages, split layout",
+                       "tokens_per_step": T, "l2": f"{R} rotating input sets > 129 MB L2",
+                       "timing": f"{K // S} replays of a CUDA graph of {S} steps"},
+            "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / world / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "k_quant_insert_kernel", "algorithmic_per_launch": nbytes,
+                         "peak_source": peaks["source"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": nbytes * world * Ke / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": T * (256 + 8), "d2h_bytes_per_step": 4},
+            "gpu_launches": K, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,6 +575,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["indexer", "kcache"], default="indexer",
+                    help="the indexer decode path (logits, top-k), or the K-cache write before it")
     ap.add_argument("--path", choices=["fused", "separate"], default="separate",
                     help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()
@@ -478,6 +597,8 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
+        if args.op == "kcache":
+            return run_kcache(args, rank, world, local_rank)
         return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:

@@ -234,6 +234,36 @@ SAI_API int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t
                               int32_t k, int32_t* indices, int64_t indices_stride,
                               uint32_t* status, sai_stream_t stream);
 
+/*
+ * sai_indexer_k_quant_insert -- quantise new K rows to FP8 and write them into
+ * the paged K-cache (one launch).  The step before the logits: the cache
+ * kernels address slots in int64 (ATOM PR 2533, "[MLA] Address Triton decode
+ * KV rows with int64 ids", section "Problem").
+ *
+ *   k_bf16        device, bf16 bits [num_tokens, head_dim], contiguous.  16-byte aligned.
+ *   num_tokens    rows of k (>= 0; 0 launches nothing and accepts null pointers).
+ *   head_dim      must be 128.
+ *   slot_mapping  device, int64 [num_tokens]: token t goes to slot
+ *                 slot_mapping[t] = page * page_size + position.  A negative
+ *                 slot writes nothing (padding); a slot at or past
+ *                 num_pages * page_size writes nothing and raises
+ *                 SAI_STATUS_BAD_PAGE.  Slots must be distinct.  8-byte aligned.
+ *   kv_cache      device, the paged cache of sai_paged_mqa_logits (num_pages
+ *                 pages of page_size * (head_dim + 4) bytes, layout kv_layout).
+ *                 Only the written tokens' bytes change.  16-byte aligned.
+ *   page_size     8, 16, 32, 64, 128 or 256.
+ *   status        nullable device uint32 word; SAI_STATUS_* bits are OR-ed in.
+ *
+ * Per token: scale = amax / 448 in fp32 (448 is the largest e4m3fn
+ * magnitude; 1 for an all-zero row); each value's byte is the e4m3fn code
+ * of the fp32 quotient value / scale, rounded to nearest, ties to even,
+ * saturating at +-448.  The scale is stored as the token's fp32 scale.
+ */
+SAI_API int sai_indexer_k_quant_insert(const uint16_t* k_bf16, int64_t num_tokens, int32_t head_dim,
+                               const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_pages,
+                               int32_t page_size, int32_t kv_layout, uint32_t* status,
+                               sai_stream_t stream);
+
 /* Static, human-readable name of a return code. */
 SAI_API const char* sai_error_string(int code);
 

@@ -24,6 +24,7 @@ __all__ = [
     "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
     "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
     "logits_topk_workspace_bytes", "paged_mqa_logits_topk", "paged_mqa_logits_topk_static",
+    "indexer_k_quant_insert",
     "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
     "KV_PAGE_SPLIT", "KV_INTERLEAVED",
 ]
@@ -75,6 +76,8 @@ _SIGS = {
                                                     _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                                     _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _c.c_int64,
                                                     _P, _P]),
+    "sai_indexer_k_quant_insert": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _P, _P, _c.c_int64, _c.c_int32,
+                                              _c.c_int32, _P, _P]),
     "sai_error_string": (_c.c_char_p, [_c.c_int]),
     "sai_version": (_c.c_int, []),
 }
@@ -234,6 +237,34 @@ def paged_mqa_logits_topk_static(q, kv_cache, page_size: int, weights, context_l
         _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_paged_mqa_logits_topk_static")
+
+
+def indexer_k_quant_insert(k, slot_mapping, kv_cache, page_size: int, *, num_pages: Optional[int] = None,
+                           kv_layout="split", status=None, stream=None) -> None:
+    """Quantise K rows to FP8 and write them into the paged cache (see
+    `sai_indexer_k_quant_insert`).
+
+    k             bfloat16 [T, 128], contiguous
+    slot_mapping  int64 [T]: page * page_size + position; negative = skip
+    kv_cache      uint8 / float8 bytes of num_pages * page_size * 132 (contiguous)
+    """
+    import torch
+
+    if k.dim() != 2 or not k.is_contiguous() or k.dtype != torch.bfloat16:
+        raise ValueError("k must be a contiguous bfloat16 [T, head_dim] tensor")
+    if slot_mapping.dim() != 1 or slot_mapping.numel() != k.shape[0]:
+        raise ValueError("slot_mapping must be [T]")
+    if not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous")
+    T, D = k.shape
+    if num_pages is None:
+        num_pages = kv_cache.numel() * kv_cache.element_size() // (page_size * (D + 4))
+    code = library().sai_indexer_k_quant_insert(
+        _ptr(k, torch.bfloat16, "k"), int(T), int(D), _ptr(slot_mapping, torch.int64, "slot_mapping"),
+        _ptr(kv_cache, (torch.uint8, torch.float8_e4m3fn), "kv_cache"), int(num_pages), int(page_size),
+        int(_LAYOUTS[kv_layout]), _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_indexer_k_quant_insert")
 
 
 def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:

@@ -184,6 +184,23 @@ int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t* kv_cac
   return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int sai_indexer_k_quant_insert(const uint16_t* k_bf16, int64_t num_tokens, int32_t head_dim,
+                               const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_pages,
+                               int32_t page_size, int32_t kv_layout, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  if (num_tokens < 0 || head_dim < 1 || num_pages < 1 || page_size < 1) return SAI_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return SAI_OK;                     // an empty batch may pass null pointers
+  if (!k_bf16 || !slot_mapping || !kv_cache) return SAI_ERR_INVALID_ARGUMENT;
+  if (kv_layout != SAI_KV_PAGE_SPLIT && kv_layout != SAI_KV_INTERLEAVED) return SAI_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim || !supported_page_size(page_size)) return SAI_ERR_UNSUPPORTED;
+  if (num_pages > (INT64_MAX / 4) / ((int64_t)page_size * kTokenBytes)) return SAI_ERR_INVALID_ARGUMENT;
+  if (num_tokens > INT64_MAX / (8 * kHeadDim)) return SAI_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_bf16, 16) || !aligned(slot_mapping, 8) || !aligned(kv_cache, 16) || !aligned(status, 4))
+    return SAI_ERR_MISALIGNED;
+  return from_cuda(launch_k_quant_insert(k_bf16, num_tokens, slot_mapping, kv_cache, num_pages, page_size, kv_layout,
+                                         status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k) {
   if (rows < 0 || max_len < 0 || k < 1) return 0;
   return sai::topk_workspace_bytes(rows, max_len, k);

@@ -77,6 +77,9 @@ struct TopKArgs {
 };
 
 cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream);
+cudaError_t launch_k_quant_insert(const uint16_t* k, int64_t num_tokens, const int64_t* slots, uint8_t* cache,
+                                  int64_t num_pages, int page_size, int layout, uint32_t* status,
+                                  cudaStream_t stream);
 size_t topk_workspace_bytes(int rows, int64_t max_len, int k);
 
 int device_sm_count();

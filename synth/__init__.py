@@ -320,3 +320,18 @@ def custom(*, batch: int, next_n: int, heads: int, page_size: int, context_lens,
 
 
 NAMED = {"tiny": tiny, "decode": decode, "mtp": mtp, "wide": wide, "kv2g": kv2g}
+
+
+# ---------------------------------------------------------------- K-cache write
+def kcache_batch(num_tokens: int, page_size: int, num_pages: int, seed: int = 5):
+    """New K rows for the K-cache write: bf16 bits [T, 128] of N(0, 1) draws
+    times a per-row factor exp(U(-2, 2)) (rows of different magnitudes), and
+    T distinct slots drawn from the pool's num_pages * page_size (int64)."""
+    import torch
+
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((num_tokens, HEAD_DIM)).astype(np.float32)
+    x *= np.exp(rng.uniform(-2, 2, (num_tokens, 1))).astype(np.float32)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slots = rng.choice(num_pages * page_size, size=num_tokens, replace=False).astype(np.int64)
+    return bits, slots

@@ -167,6 +167,31 @@ def test_fused_argument_validation(lib, kw, code):
     assert _fused(lib, **kw) == code
 
 
+def _quant(lib, **kw):
+    args = dict(k=A16, T=10, D=128, slots=A16, cache=A16, num_pages=4, P=16, layout=0, status=None)
+    args.update(kw)
+    return lib.sai_indexer_k_quant_insert(args["k"], args["T"], args["D"], args["slots"], args["cache"],
+                                          args["num_pages"], args["P"], args["layout"], args["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), sai.ERR_INVALID_ARGUMENT),
+    (dict(k=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(slots=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(cache=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(num_pages=0), sai.ERR_INVALID_ARGUMENT),
+    (dict(layout=3), sai.ERR_INVALID_ARGUMENT),
+    (dict(D=64), sai.ERR_UNSUPPORTED),
+    (dict(P=12), sai.ERR_UNSUPPORTED),
+    (dict(k=A16 + 8), sai.ERR_MISALIGNED),
+    (dict(slots=A16 + 4), sai.ERR_MISALIGNED),
+    (dict(cache=A16 + 4), sai.ERR_MISALIGNED),
+    (dict(T=0), sai.OK),
+])
+def test_kcache_argument_validation(lib, kw, code):
+    assert _quant(lib, **kw) == code
+
+
 def test_workspace_query(lib):
     n = lib.sai_top_k_workspace_bytes(1024, 32768, 2048)
     assert n >= 0
