@@ -20,13 +20,15 @@ result for comparison):
 * `kcache.quantize_k_rows` / `kcache.insert_k_rows`: the K-cache write that
   precedes the path: per-token FP8 quantisation (scale = amax / 448) and
   insertion into the paged cache through int64 slots.
+* `gather.kv_row_ids` / `gather.gather_kv_rows`: the consumer's gather of
+  the selected tokens' KV rows through int64 row ids.
 
 Parity status: every function here is pinned by `tests/test_oracle_*.py`
 against facts fixed outside this code (a library FP8 conversion, exact
 rational brute force, closed forms, invariants, a library sort, the byte
 values printed for the reproducer).  No function is "parity unpinned".
 """
-from . import kcache  # noqa: F401
+from . import gather, kcache  # noqa: F401
 from .indexer import (  # noqa: F401
     E4M3FN_NAN_CODES,
     e4m3fn_table,
