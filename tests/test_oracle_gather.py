@@ -34,16 +34,17 @@ def test_gathered_rows_spell_their_row_ids():
 
 
 def test_offsets_past_the_int32_limit_are_exact():
-    # Block 233,016 of 16 tokens is the first whose MLA rows start past
-    # 2^31 bytes; the last token of block 233,015 is the last below.
+    # 2^31 / 576 = 3,728,270.2: row 3,728,270 (block 233,016, position 14)
+    # is the last whose MLA offset fits in int32; row 3,728,271 (position 15)
+    # is the first past it.
     P = 16
-    table = np.array([[233015, 233016, 240000]])
-    ids = gather.kv_row_ids(np.array([[15, 16, 40]]), table, 1, P, 250000)
-    assert ids.tolist() == [[233015 * 16 + 15, 233016 * 16, 240000 * 16 + 8]]
+    table = np.array([[233016, 240000]])
+    ids = gather.kv_row_ids(np.array([[14, 15, 24]]), table, 1, P, 250000)
+    assert ids.tolist() == [[3728270, 3728271, 240000 * 16 + 8]]
     offs = [int(j) * MLA_ROW for j in ids[0]]
-    assert offs[0] + MLA_ROW <= 2 ** 31 < offs[1]
+    assert offs[0] < 2 ** 31 < offs[1]
     wrapped = [(o + 2 ** 31) % 2 ** 32 - 2 ** 31 for o in offs]             # what an int32 product gives
-    assert wrapped[1] < 0 and wrapped[2] < 0 and wrapped[0] == offs[0]
+    assert wrapped[0] == offs[0] and wrapped[1] < 0 and wrapped[2] < 0
 
 
 def test_padding_and_bad_entries_give_zero_rows():
