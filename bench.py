@@ -567,6 +567,121 @@ def run_kcache(args, rank: int, world: int, local_rank: int):
     return 0
 
 
+# ------------------------------------------------------------------ consumer gather
+GA_METRIC = "selected-KV gather GB/s (top-k indices -> int64 row ids -> 576-byte rows), 1 GB300"
+GA_ROW, GA_PAGE, GA_PAGES = 576, 64, 8192            # FP8 MLA rows, the decode pool's pages
+
+
+def run_gather(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import sparse_attention_indexer_03_gb300 as sai
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    sai.build()
+    dev = torch.device("cuda", local_rank)
+    idx, table, ctx = synth.gather_batch(page_size=GA_PAGE, num_pages=GA_PAGES)
+    rows, k = idx.shape
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6)
+    pool = torch.randint(0, 256, (GA_PAGES * GA_PAGE * GA_ROW,), dtype=torch.uint8, device=dev, generator=gen)
+    out_bytes = rows * k * GA_ROW
+    R = max(2, math.ceil(2.0 * L2_BYTES / out_bytes))
+    sets = [(torch.from_numpy(idx).to(dev), torch.from_numpy(table).to(dev),
+             torch.empty((rows, k), dtype=torch.int64, device=dev),
+             torch.empty((rows, k, GA_ROW), dtype=torch.uint8, device=dev)) for _ in range(R)]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        d_idx, d_tab, ids, out = sets[i % R]
+        sai.gather_selected_kv(d_idx, 1, d_tab, GA_PAGE, pool, GA_ROW, row_ids=ids, out=out, status=status,
+                               stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    S = K if K <= 200 else 100
+    K = S * math.ceil(K / S)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(S):
+            step(i)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(K // S):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    ms, _ = aggregate(t0.elapsed_time(t1), rows, world, dev)
+    assert int(status.item()) == 0
+    # Algorithmic bytes: the selected rows read, every output row written, the
+    # indices read and the row ids written (table reads are a few KB).
+    selected = int((idx >= 0).sum())
+    nbytes = selected * GA_ROW + out_bytes + rows * k * (4 + 8)
+    # End to end: pinned indices in, gathered rows out.
+    h_idx = torch.from_numpy(idx).pin_memory()
+    h_out = torch.empty((rows, k, GA_ROW), dtype=torch.uint8).pin_memory()
+    d_idx, d_tab, ids, out = sets[0]
+    Ke = min(args.steps, 50)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(Ke + 3):
+            if i == 3:
+                e0.record(stream)
+            d_idx.copy_(h_idx, non_blocking=True)
+            sai.gather_selected_kv(d_idx, 1, d_tab, GA_PAGE, pool, GA_ROW, row_ids=ids, out=out, status=status,
+                                   stream=stream)
+            h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms, _ = aggregate(e0.elapsed_time(e1), rows, world, dev)
+    if rank != 0:
+        return 0
+    peaks = load_peaks()
+    gbs = nbytes * world * K / (ms * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        host_pool = pool[: 1 << 26].cpu().numpy()                   # a 64 MB slice of the pool
+        sub = idx[:4] % (host_pool.size // GA_ROW // GA_PAGE * GA_PAGE)
+        sub_tab = (table[:4] % (host_pool.size // GA_ROW // GA_PAGE)).astype(np.int32)
+        c0, reps = time.perf_counter(), 0
+        while time.perf_counter() - c0 < 5.0:
+            ids_h = oracle.gather.kv_row_ids(sub, sub_tab, 1, GA_PAGE, host_pool.size // GA_ROW // GA_PAGE)
+            oracle.gather.gather_kv_rows(host_pool, ids_h, GA_ROW)
+            reps += 1
+        csec = time.perf_counter() - c0
+        per = int((sub >= 0).sum()) * GA_ROW + sub.size * (GA_ROW + 12)
+        cpu = {"value": per * reps / csec / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{reps} x 4 rows of 2048 selected tokens gathered, {csec:.1f} s"}
+    line = {"metric": GA_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": f"gather: {rows} rows x k={k}, {GA_ROW}-byte rows, P={GA_PAGE}, "
+                                   f"pool {GA_PAGES} pages ({GA_PAGES * GA_PAGE * GA_ROW >> 20} MB)",
+                       "selected_rows_per_step": selected, "l2": f"{R} rotating output sets > 129 MB L2",
+                       "timing": f"{K // S} replays of a CUDA graph of {S} steps"},
+            "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / world / peaks["hbm_gbs"], "traffic": None, "kernel": "gather_rows_kernel",
+                         "algorithmic_per_launch": nbytes, "peak_source": peaks["source"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": nbytes * world * Ke / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": idx.nbytes, "d2h_bytes_per_step": out_bytes},
+            "gpu_launches": K, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -575,8 +690,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["indexer", "kcache"], default="indexer",
-                    help="the indexer decode path (logits, top-k), or the K-cache write before it")
+    ap.add_argument("--op", choices=["indexer", "kcache", "gather"], default="indexer",
+                    help="the indexer decode path (logits, top-k), the K-cache write before it, "
+                         "or the consumer's gather of the selected KV rows after it")
     ap.add_argument("--path", choices=["fused", "separate"], default="separate",
                     help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()
@@ -599,6 +715,8 @@ def main():
     try:
         if args.op == "kcache":
             return run_kcache(args, rank, world, local_rank)
+        if args.op == "gather":
+            return run_gather(args, rank, world, local_rank)
         return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:

@@ -264,6 +264,40 @@ SAI_API int sai_indexer_k_quant_insert(const uint16_t* k_bf16, int64_t num_token
                                int32_t page_size, int32_t kv_layout, uint32_t* status,
                                sai_stream_t stream);
 
+/*
+ * sai_gather_selected_kv -- the consumer's gather of the selected tokens' KV
+ * rows (one launch).  Row ids are formed and multiplied by the row size in
+ * 64 bits (ATOM PR 2533, "[MLA] Address Triton decode KV rows with int64
+ * ids": an int32 product wraps past row 2^31 / 576).
+ *
+ *   indices       device, int32 [rows, indices_stride] (>= k): token
+ *                 positions, as written by sai_top_k_per_row_decode; -1 = none.
+ *   rows, k       query rows (>= 0; 0 launches nothing) and entries per row.
+ *   next_n        rows per request: row r belongs to request r / next_n.
+ *   block_table   device, int32 [rows / next_n, block_table_stride]: token t of
+ *                 a request is at position t % page_size of page
+ *                 block_table[b, t / page_size].
+ *   page_size     tokens per page of the KV pool, 1 .. 65536.
+ *   kv_pool       device, token-major rows: row id j = page * page_size +
+ *                 position occupies bytes [j * row_bytes, (j + 1) * row_bytes).
+ *                 16-byte aligned; may be null when out is null.
+ *   num_pages     pages in the pool (page ids are checked against it).
+ *   row_bytes     bytes per KV row: a multiple of 16, at most 4096 (576 for
+ *                 an FP8 MLA row).
+ *   row_ids       nullable device int64 [rows, k]: the selected row ids, -1
+ *                 for a -1 index or a bad table entry.  8-byte aligned.
+ *   out           nullable device [rows, k, row_bytes]: the selected rows, all
+ *                 zero where the row id is -1.  16-byte aligned.
+ *   status        nullable device word: SAI_STATUS_BAD_PAGE for an index whose
+ *                 table entry lies past the table row or names a page outside
+ *                 the pool.
+ * At least one of row_ids and out must be non-null.
+ */
+SAI_API int sai_gather_selected_kv(const int32_t* indices, int64_t indices_stride, int32_t rows, int32_t k,
+                           int32_t next_n, const int32_t* block_table, int64_t block_table_stride,
+                           int32_t page_size, const uint8_t* kv_pool, int64_t num_pages, int32_t row_bytes,
+                           int64_t* row_ids, uint8_t* out, uint32_t* status, sai_stream_t stream);
+
 /* Static, human-readable name of a return code. */
 SAI_API const char* sai_error_string(int code);
 

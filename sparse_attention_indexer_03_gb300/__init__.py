@@ -24,7 +24,7 @@ __all__ = [
     "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
     "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
     "logits_topk_workspace_bytes", "paged_mqa_logits_topk", "paged_mqa_logits_topk_static",
-    "indexer_k_quant_insert",
+    "indexer_k_quant_insert", "gather_selected_kv",
     "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
     "KV_PAGE_SPLIT", "KV_INTERLEAVED",
 ]
@@ -78,6 +78,8 @@ _SIGS = {
                                                     _P, _P]),
     "sai_indexer_k_quant_insert": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _P, _P, _c.c_int64, _c.c_int32,
                                               _c.c_int32, _P, _P]),
+    "sai_gather_selected_kv": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _P, _c.c_int64,
+                                          _c.c_int32, _P, _c.c_int64, _c.c_int32, _P, _P, _P, _P]),
     "sai_error_string": (_c.c_char_p, [_c.c_int]),
     "sai_version": (_c.c_int, []),
 }
@@ -265,6 +267,41 @@ def indexer_k_quant_insert(k, slot_mapping, kv_cache, page_size: int, *, num_pag
         int(_LAYOUTS[kv_layout]), _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_indexer_k_quant_insert")
+
+
+def gather_selected_kv(indices, next_n: int, block_table, page_size: int, kv_pool, row_bytes: int, *,
+                       row_ids=None, out=None, num_pages: Optional[int] = None, status=None,
+                       stream=None) -> None:
+    """Gather the selected tokens' KV rows and/or their int64 row ids (see
+    `sai_gather_selected_kv`).
+
+    indices      int32 [rows, >= k] (row stride from the tensor); k = indices.shape[1]
+    block_table  int32 [rows / next_n, stride] (inner stride 1)
+    kv_pool      uint8 bytes of num_pages * page_size * row_bytes (contiguous)
+    row_ids      optional int64 [rows, k], contiguous
+    out          optional uint8 [rows, k, row_bytes], contiguous
+    """
+    import torch
+
+    if indices.dim() != 2 or indices.stride(1) != 1:
+        raise ValueError("indices must be [rows, k] with unit inner stride")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, stride] with unit inner stride")
+    rows, k = indices.shape
+    if out is not None and (not out.is_contiguous() or out.numel() * out.element_size() < rows * k * row_bytes):
+        raise ValueError("out must be a contiguous [rows, k, row_bytes] byte tensor")
+    if row_ids is not None and (not row_ids.is_contiguous() or row_ids.numel() < rows * k):
+        raise ValueError("row_ids must be a contiguous [rows, k] int64 tensor")
+    if num_pages is None:
+        num_pages = kv_pool.numel() * kv_pool.element_size() // (page_size * row_bytes)
+    code = library().sai_gather_selected_kv(
+        _ptr(indices, torch.int32, "indices"), int(indices.stride(0)), int(rows), int(k), int(next_n),
+        _ptr(block_table, torch.int32, "block_table"), int(block_table.stride(0)), int(page_size),
+        _ptr(kv_pool, None, "kv_pool"), int(num_pages), int(row_bytes),
+        _ptr(row_ids, torch.int64, "row_ids"), _ptr(out, None, "out"),
+        _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_gather_selected_kv")
 
 
 def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:

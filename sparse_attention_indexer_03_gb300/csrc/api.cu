@@ -201,6 +201,32 @@ int sai_indexer_k_quant_insert(const uint16_t* k_bf16, int64_t num_tokens, int32
                                          status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int sai_gather_selected_kv(const int32_t* indices, int64_t indices_stride, int32_t rows, int32_t k, int32_t next_n,
+                           const int32_t* block_table, int64_t block_table_stride, int32_t page_size,
+                           const uint8_t* kv_pool, int64_t num_pages, int32_t row_bytes, int64_t* row_ids,
+                           uint8_t* out, uint32_t* status, sai_stream_t stream) {
+  using namespace sai;
+  if (rows < 0 || k < 1 || next_n < 1 || indices_stride < k || block_table_stride < 1 || page_size < 1 ||
+      num_pages < 1 || row_bytes < 1)
+    return SAI_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return SAI_OK;
+  if (!indices || !block_table || (!row_ids && !out) || (out && !kv_pool)) return SAI_ERR_INVALID_ARGUMENT;
+  if (row_bytes % 16 != 0 || row_bytes > 4096 || page_size > 65536) return SAI_ERR_UNSUPPORTED;
+  if (num_pages > (INT64_MAX / 4) / ((int64_t)page_size * row_bytes)) return SAI_ERR_INVALID_ARGUMENT;
+  if (indices_stride > (INT64_MAX / 8) / ((int64_t)rows + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if (block_table_stride > (INT64_MAX / 8) / ((int64_t)rows + 1)) return SAI_ERR_INVALID_ARGUMENT;
+  if ((int64_t)rows * k > INT64_MAX / 4096) return SAI_ERR_INVALID_ARGUMENT;
+  if (!aligned(indices, 4) || !aligned(block_table, 4) || !aligned(kv_pool, 16) || !aligned(row_ids, 8) ||
+      !aligned(out, 16) || !aligned(status, 4))
+    return SAI_ERR_MISALIGNED;
+  GatherArgs a;
+  a.indices = indices; a.idx_stride = indices_stride; a.rows = rows; a.k = k; a.next_n = next_n;
+  a.block_table = block_table; a.bt_stride = block_table_stride; a.page_size = page_size;
+  a.pool = kv_pool; a.num_pages = num_pages; a.row_bytes = row_bytes; a.row_ids = row_ids; a.out = out;
+  a.status = status;
+  return from_cuda(launch_gather_rows(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t k) {
   if (rows < 0 || max_len < 0 || k < 1) return 0;
   return sai::topk_workspace_bytes(rows, max_len, k);

@@ -77,6 +77,21 @@ struct TopKArgs {
 };
 
 cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream);
+struct GatherArgs {
+  const int32_t* indices;     // [rows, idx_stride]
+  int64_t idx_stride;
+  int32_t rows, k, next_n;
+  const int32_t* block_table; // [rows / next_n, bt_stride]
+  int64_t bt_stride;
+  int32_t page_size;
+  const uint8_t* pool;        // token-major rows of row_bytes
+  int64_t num_pages;
+  int32_t row_bytes;
+  int64_t* row_ids;           // [rows, k] or null
+  uint8_t* out;               // [rows, k, row_bytes] or null
+  uint32_t* status;
+};
+cudaError_t launch_gather_rows(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_k_quant_insert(const uint16_t* k, int64_t num_tokens, const int64_t* slots, uint8_t* cache,
                                   int64_t num_pages, int page_size, int layout, uint32_t* status,
                                   cudaStream_t stream);

@@ -335,3 +335,22 @@ def kcache_batch(num_tokens: int, page_size: int, num_pages: int, seed: int = 5)
     bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     slots = rng.choice(num_pages * page_size, size=num_tokens, replace=False).astype(np.int64)
     return bits, slots
+
+
+# ---------------------------------------------------------------- consumer gather
+def gather_batch(batch: int = 64, next_n: int = 1, k: int = 2048, page_size: int = 64,
+                 num_pages: int = 8192, max_ctx: int = 8192, seed: int = 6):
+    """Selected token positions as the top-k leaves them, for the decode
+    shapes: context lengths U[1024, max_ctx], a block table that is one
+    permutation of the pool reshaped [batch, num_pages / batch], and for each
+    row a sorted random subset of min(k, ctx_r) positions, padded with -1.
+    Returns (indices int32 [batch * next_n, k], block_table int32, context_lens)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(1024, max_ctx, size=batch, endpoint=True)
+    table = rng.permutation(num_pages).reshape(batch, num_pages // batch).astype(np.int32)
+    idx = np.full((batch * next_n, k), -1, np.int32)
+    for r in range(batch * next_n):
+        n = max(0, int(ctx[r // next_n]) - next_n + r % next_n + 1)
+        m = min(k, n)
+        idx[r, :m] = np.sort(rng.choice(n, m, replace=False))
+    return idx, table, ctx

@@ -192,6 +192,35 @@ def test_kcache_argument_validation(lib, kw, code):
     assert _quant(lib, **kw) == code
 
 
+def _gather(lib, **kw):
+    args = dict(idx=A4, idx_stride=64, rows=2, k=64, next_n=1, bt=A4, bt_stride=8, P=16, pool=A16,
+                num_pages=10, row_bytes=576, ids=A16, out=A16, status=None)
+    args.update(kw)
+    return lib.sai_gather_selected_kv(args["idx"], args["idx_stride"], args["rows"], args["k"], args["next_n"],
+                                      args["bt"], args["bt_stride"], args["P"], args["pool"], args["num_pages"],
+                                      args["row_bytes"], args["ids"], args["out"], args["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), sai.ERR_INVALID_ARGUMENT),
+    (dict(k=0), sai.ERR_INVALID_ARGUMENT),
+    (dict(idx_stride=63), sai.ERR_INVALID_ARGUMENT),
+    (dict(idx=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(bt=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(ids=None, out=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(pool=None), sai.ERR_INVALID_ARGUMENT),
+    (dict(row_bytes=100), sai.ERR_UNSUPPORTED),
+    (dict(row_bytes=8192), sai.ERR_UNSUPPORTED),
+    (dict(pool=A16 + 8), sai.ERR_MISALIGNED),
+    (dict(out=A16 + 8), sai.ERR_MISALIGNED),
+    (dict(ids=A16 + 4), sai.ERR_MISALIGNED),
+    (dict(idx=A4 + 2), sai.ERR_MISALIGNED),
+    (dict(rows=0), sai.OK),
+])
+def test_gather_argument_validation(lib, kw, code):
+    assert _gather(lib, **kw) == code
+
+
 def test_workspace_query(lib):
     n = lib.sai_top_k_workspace_bytes(1024, 32768, 2048)
     assert n >= 0
