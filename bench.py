@@ -84,13 +84,13 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def make_workload(name: str):
+def make_workload(name: str, layout: str = "split"):
     import synth
 
     if name.startswith("sweep:"):
         p, n, h, b, c = (int(x) for x in name.split(":", 1)[1].split(","))
-        return synth.sweep_point(p, n, h, b, c)
-    return synth.NAMED[name]()
+        return synth.sweep_point(p, n, h, b, c, layout=layout)
+    return synth.NAMED[name](layout)
 
 
 def describe(w) -> str:
@@ -180,10 +180,10 @@ def aggregate(ms: float, tokens: int, world: int, device=None):
     return float(t.item()), int(n.item())
 
 
-def rank_workload(name: str, rank: int):
+def rank_workload(name: str, rank: int, layout: str = "split"):
     """The batch of requests rank `rank` serves: the named workload (the same
     shapes on every rank, weak scaling)."""
-    return make_workload(name)
+    return make_workload(name, layout)
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -254,7 +254,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(local_rank)
     sai.build()
     dev = torch.device("cuda", local_rank)
-    w = rank_workload(args.workload, rank)
+    w = rank_workload(args.workload, rank, args.layout)
     tok = row_tokens(w)
 
     # Rotating input sets: enough that one cycle touches more bytes than L2.
@@ -275,7 +275,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def logits_call(d):
         sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
                              d["block_table"], d["logits"], w.max_model_len, num_pages=w.pool.num_pages,
-                             status=status, stream=stream)
+                             status=status, kv_layout=w.layout, stream=stream)
 
     def topk_call(d):
         sai.top_k_per_row_decode(d["logits"], d["context_lens"], w.next_n, w.max_model_len, w.topk,
@@ -415,8 +415,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         roof = {"bound": "tensor", "achieved": lflops / (lg_ms * 1e-3) / 1e12, "peak": fp8_peak_tflops,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic(w.name, fused)
-    roof["kernel"] = "logits_tc_kernel" + (" (fused top-k)" if fused else "")
+    simt = w.layout == "interleaved"
+    roof["traffic"] = None if simt else profiled_traffic(w.name, fused)
+    roof["kernel"] = "logits_simt_kernel" if simt else "logits_tc_kernel" + (" (fused top-k)" if fused else "")
     roof["algorithmic_per_launch"] = lbytes if roof["bound"] == "hbm" else lflops
     roof["peak_source"] = peaks["source"] + (" (fp8 = 2 x measured bf16)" if roof["bound"] == "tensor" else "")
     value = tok_all * K / (ms * 1e-3) / 1e9
@@ -693,6 +694,8 @@ def main():
     ap.add_argument("--op", choices=["indexer", "kcache", "gather"], default="indexer",
                     help="the indexer decode path (logits, top-k), the K-cache write before it, "
                          "or the consumer's gather of the selected KV rows after it")
+    ap.add_argument("--layout", choices=["split", "interleaved"], default="split",
+                    help="K-cache layout of the indexer workload (interleaved: the CUDA-core path)")
     ap.add_argument("--path", choices=["fused", "separate"], default="separate",
                     help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()

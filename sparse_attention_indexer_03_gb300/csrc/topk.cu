@@ -12,7 +12,9 @@
 //
 // The kernel is launched as a programmatic dependent of the previous kernel
 // in the stream (the logits launch): it may start while that kernel drains,
-// and waits for it to complete before reading any logits.
+// and waits for it to complete before reading any logits.  It then lets its
+// own dependents start at once: with one CTA per row, a decode batch leaves
+// most SMs free, where the next launch can run its set-up.
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,6 +48,7 @@ topk_reg_kernel(TopKArgs a) {
   extern __shared__ uint32_t hist_smem[];
   __shared__ SelectShared<kThreads> sh;
   ptx::wait_prerequisites();
+  ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
   const int tid = threadIdx.x;
   const int64_t r = blockIdx.x;
   const float* row = a.logits + r * a.stride;              // 64-bit row base
@@ -88,6 +91,7 @@ topk_smem_kernel(TopKArgs a) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
   __shared__ SelectShared<kThreads> sh;
   ptx::wait_prerequisites();
+  ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
   const int64_t r = blockIdx.x;
   const int64_t n = row_len(a, r);
   int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
