@@ -1,7 +1,7 @@
 // Per-row top-k of the indexer logits (`top_k_per_row_decode`, run right after
 // the logits launch in aiter PR 4244, opening paragraph).
 //
-// One CTA of 512 threads per row runs the exact radix select of select.cuh
+// One CTA of 1024 threads per row runs the exact radix select of select.cuh
 // and writes the row's indices in a deterministic order: the columns strictly
 // above the threshold, ascending, then the ties at the threshold, lowest
 // columns first.  Rows of a logical width up to 16384 are held in registers
@@ -24,7 +24,7 @@
 namespace sai {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ int64_t row_len(const TopKArgs& a, int64_t r) {
@@ -136,12 +136,11 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.batch * a.next_n;
   if (rows == 0) return cudaSuccess;
   const unsigned g = (unsigned)rows;
-  static int set4[64], set8[64], set16[64], set32[64], set_smem[64];
+  static int set4[64], set8[64], set16[64], set_smem[64];
   cudaError_t e;
   if (a.width <= 4 * kThreads) e = launch_pdl(topk_reg_kernel<4>, g, a, stream, set4, kSelectSmem, kSelectSmem);
   else if (a.width <= 8 * kThreads) e = launch_pdl(topk_reg_kernel<8>, g, a, stream, set8, kSelectSmem, kSelectSmem);
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
-  else if (a.width <= 32 * kThreads) e = launch_pdl(topk_reg_kernel<32>, g, a, stream, set32, kSelectSmem, kSelectSmem);
   else e = launch_pdl(topk_smem_kernel, g, a, stream, set_smem,
                      kSelectSmem + 4 * (size_t)(std::min<int64_t>(a.width, kSmemKeys) + 4), kSmemKeysBytes);
   if (e != cudaSuccess) return e;
