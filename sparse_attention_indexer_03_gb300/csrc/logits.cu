@@ -463,8 +463,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       ptx::prefetch_tensormap(&tmap_kv);
       ptx::prefetch_tensormap(&tmap_q);
     }
-    // Inputs may come from the previous kernel in the stream, and the logits
-    // buffer may still be read by it: wait for it before touching either.
+    // The context lengths' lines are pulled into L2 first (a prefetch returns
+    // nothing, so it may run while the previous kernel still works); then,
+    // since inputs may come from that kernel and the logits buffer may still
+    // be read by it, wait for it before touching either.
+    for (int64_t x = (int64_t)lane * 32; x < p.batch; x += 32 * 32) ptx::prefetch_l2(p.context_lens + x);
     ptx::wait_prerequisites();
     compute_partition<NEXT_N>(p, part, ctx_s, lane);
   } else if (warp == 1) {
