@@ -139,11 +139,12 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
 
 // Ordered compaction of the selection over keys key_at(i), i in [0, n): warp w
 // owns columns [w * seg, (w + 1) * seg); two sweeps (count, then write), each
-// reading kU chunks of 32 keys before using them so the reads overlap.
+// reading kU chunks of 32 keys before using them so the reads overlap (16
+// coalesced loads in flight per thread).
 template <int NT, typename Bar, typename KeyAt>
 __device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const SelectResult& s, int64_t n, int k,
                                                int32_t* out, int tid, Bar bar, KeyAt key_at) {
-  constexpr int kW = NT / 32, kU = 4;
+  constexpr int kW = NT / 32, kU = 16;
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t n_gt = (uint32_t)k - s.remaining;
   const int64_t seg = ((n + kW - 1) / kW + 31) / 32 * 32;
@@ -260,21 +261,32 @@ struct SmemRun {
 
 // Top-k of one row read from global memory (through L2: written by other
 // CTAs of the same launch, or by an earlier kernel).  Row length n > k.
-// Each thread reads kU keys before counting them, so the reads overlap.
+// The radix passes read the row as 16-byte vectors, consecutive threads on
+// consecutive vectors, eight in flight per thread (a few scalar columns
+// before the first 16-byte boundary and after the last).
 template <int NT, typename Bar>
 __device__ __forceinline__ void topk_row_stream(const float* row, int64_t n, int k, int32_t* out,
                                                 SelectShared<NT>& sh, uint32_t* hist, int tid, Bar bar) {
-  constexpr int kU = 8;
+  constexpr int kV = 8;
+  const int64_t head = min(n, (int64_t)(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 2));
+  const float4* vec = reinterpret_cast<const float4*>(row + head);
+  const int64_t nv = (n - head) >> 2, tail0 = head + 4 * nv;
   auto for_each = [&](auto&& f) {
-    for (int64_t base = 0; base < n; base += (int64_t)NT * kU) {
-      uint32_t key[kU];
+    if (tid < head) f(true, float_key(__ldcg(row + tid)));
+    for (int64_t b = 0; b < nv; b += (int64_t)NT * kV) {
+      float4 x[kV];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        key[u] = float_key(__ldcg(row + min(base + u * NT + tid, n - 1)));
+      for (int u = 0; u < kV; ++u) x[u] = __ldcg(vec + min(b + u * NT + tid, nv - 1));
+#pragma unroll
+      for (int u = 0; u < kV; ++u) {
+        const bool v = b + u * NT + tid < nv;
+        f(v, float_key(x[u].x));
+        f(v, float_key(x[u].y));
+        f(v, float_key(x[u].z));
+        f(v, float_key(x[u].w));
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) f(base + u * NT + tid < n, key[u]);
     }
+    for (int64_t i = tail0 + tid; i < n; i += NT) f(true, float_key(__ldcg(row + i)));
   };
   const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each);
   compact_stream<NT>(sh, s, n, k, out, tid, bar, [&](int64_t i) { return float_key(__ldcg(row + i)); });
