@@ -713,9 +713,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
 #pragma unroll
       for (int jr = 0; jr < K::ROWS; ++jr) {
         const float4* wrow = w0 + jr * (H / 4);
-        // Eight independent partial sums: one dependent chain of H fused
-        // multiply-adds would bound the epilogue by FMA latency.
-        float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // Eight independent partial sums, held as four pairs updated by
+        // paired fp32 FMAs: one dependent chain of H fused multiply-adds would
+        // bound the epilogue by FMA latency.
+        float2 part[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
         for (int h0 = 0; h0 < H; h0 += 64) {         // two 32-column TMEM loads, one wait
           uint32_t v[64];
@@ -727,14 +729,17 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            float* q4 = part + 4 * (x & 1);
-            q4[0] = fmaf(w4[x].x, fmaxf(__uint_as_float(v[4 * x + 0]), 0.f), q4[0]);
-            q4[1] = fmaf(w4[x].y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), q4[1]);
-            q4[2] = fmaf(w4[x].z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), q4[2]);
-            q4[3] = fmaf(w4[x].w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), q4[3]);
+            float2* q = part + 2 * (x & 1);
+            const float2 r01 = make_float2(fmaxf(__uint_as_float(v[4 * x + 0]), 0.f),
+                                           fmaxf(__uint_as_float(v[4 * x + 1]), 0.f));
+            const float2 r23 = make_float2(fmaxf(__uint_as_float(v[4 * x + 2]), 0.f),
+                                           fmaxf(__uint_as_float(v[4 * x + 3]), 0.f));
+            q[0] = __ffma2_rn(make_float2(w4[x].x, w4[x].y), r01, q[0]);
+            q[1] = __ffma2_rn(make_float2(w4[x].z, w4[x].w), r23, q[1]);
           }
         }
-        out[jr] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+        out[jr] = ((part[0].x + part[0].y) + (part[1].x + part[1].y)) +
+                  ((part[2].x + part[2].y) + (part[3].x + part[3].y));
       }
       ptx::tc_fence_before();
       __syncwarp();
