@@ -474,9 +474,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         roof = {"bound": "tensor", "achieved": lflops / (lg_ms * 1e-3) / 1e12, "peak": fp8_peak_tflops,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    simt = w.layout == "interleaved"
-    roof["traffic"] = None if simt else profiled_traffic(w.name, fused)
-    roof["kernel"] = "logits_simt_kernel" if simt else "logits_tc_kernel" + (" (fused top-k)" if fused else "")
+    il = w.layout == "interleaved"
+    roof["traffic"] = None if il else profiled_traffic(w.name, fused)
+    roof["kernel"] = "logits_tc_kernel" + (" (interleaved K)" if il else "") + (" (fused top-k)" if fused else "")
     roof["algorithmic_per_launch"] = lbytes if roof["bound"] == "hbm" else lflops
     roof["peak_source"] = peaks["source"] + (" (fp8 = 2 x measured bf16)" if roof["bound"] == "tensor" else "")
     value = tok_all * K / (ms * 1e-3) / 1e9
@@ -757,12 +757,15 @@ def main():
                     help="the indexer decode path (logits, top-k), the K-cache write before it, "
                          "or the consumer's gather of the selected KV rows after it")
     ap.add_argument("--layout", choices=["split", "interleaved"], default="split",
-                    help="K-cache layout of the indexer workload (interleaved: the CUDA-core path)")
+                    help="K-cache layout of the indexer workload (interleaved: pages staged as stored, "
+                         "rewritten for the MMA)")
     ap.add_argument("--path", choices=["fused", "separate"], default="separate",
                     help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.path == "fused" and args.layout != "split":
+        ap.error("the fused logits + top-k launch reads page-split caches only")
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

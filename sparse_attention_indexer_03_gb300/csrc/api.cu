@@ -125,10 +125,10 @@ int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t 
                               max_model_len, kv_layout, status, a);
   if (rc != SAI_OK || batch == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // Tensor cores for the page-split layout; its 132-byte token stride makes
-  // the interleaved layout unreachable for tiled TMA, so it runs on the CUDA cores.
+  // The interleaved layout's 132-byte token pitch is no tensor-map stride:
+  // its pages come in as bulk copies and are rewritten into the MMA layout.
   if (kv_layout == SAI_KV_PAGE_SPLIT) return from_cuda(launch_logits_tc(a, st));
-  return from_cuda(launch_logits_simt(a, st));
+  return from_cuda(launch_logits_tc_interleaved(a, st));
 }
 
 size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch) {

@@ -61,8 +61,8 @@ struct LogitsArgs {
   int32_t* req_counter = nullptr;
 };
 
-cudaError_t launch_logits_simt(const LogitsArgs& a, cudaStream_t stream);
 cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream);
+cudaError_t launch_logits_tc_interleaved(const LogitsArgs& a, cudaStream_t stream);
 
 struct TopKArgs {
   const float* logits;

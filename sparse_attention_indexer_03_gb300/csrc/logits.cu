@@ -17,9 +17,16 @@
 //              256-token page.  A copy instruction costs the issuing warp
 //              hundreds of cycles whatever its size, so a tile's page copies
 //              go out as one warp-wide instruction (one lane per page) and
-//              three warps issue in parallel.  Warp 0 also computes the work partition.  Q
-//              [next_n * H, 128] of each request is loaded once into one of
-//              two Q slots.
+//              three warps issue in parallel (two where the ring is too
+//              shallow for three: see ring_waits_unambiguous).  Warp 0 also
+//              computes the work partition.  Q [next_n * H, 128] of each
+//              request is loaded once into one of two Q slots.
+//              Interleaved caches (IL; each token's 128 value bytes, then its
+//              4 scale bytes, as the aiter PR 4244 reproducer builds them):
+//              the 132-byte token pitch is no tensor-map stride, so a lane
+//              bulk-copies its page as stored into a staging slot, and once
+//              the tile has landed the warp rewrites it into the stage layout
+//              above; the MMA and the epilogue are the same.
 //   warp 3     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
 //              A = the K stage (128 tokens x 128 B, K-major, 128-byte
 //              swizzle), B = Q (whole rows j, <= 256 columns per job), fp32
@@ -50,7 +57,7 @@ namespace sai {
 namespace {
 
 constexpr int kTile = 128;                       // tokens per MMA tile (M)
-constexpr int kProducers = 3;                    // producer warps 0 .. kProducers - 1
+constexpr int kProducers = 3;                    // warps 0 .. kProducers - 1 may produce
 constexpr int kMmaWarp = kProducers;             // then the MMA warp
 constexpr int kFirstEpiWarp = kProducers + 1;    // then two epilogue warpgroups
 constexpr int kEpiWarps = 8;
@@ -89,7 +96,35 @@ struct TcParams {
 // shared memory by the partition, so the walks over requests read them there.
 constexpr int kCtxSmem = 512;
 
-template <int NEXT_N, int H>
+constexpr int kStgBytes = kTile * kTokenBytes;   // one tile of interleaved pages as stored: 16,896 B
+
+// The producers wait for a stage's release by phase parity, which cannot tell
+// the release of the stage's use u - 1 from that of use u - 2: the wait is
+// sound only if use u - 2 is known released when it starts.  A producer warp
+// has seen the releases of its own earlier tiles' predecessors (tiles
+// i - m * producers - stages, m >= 1).  Releases come from the epilogue
+// warpgroups: when a tile is several jobs, every release needs both
+// warpgroups, so releases complete in tile order and stages >= producers is
+// enough; when a tile is one job, the two warpgroups take alternate tiles and
+// only releases two tiles apart are ordered, so some m must leave
+// stages - m * producers even and non-negative.
+constexpr bool ring_waits_unambiguous(int stages, int producers, int jobs_per_tile) {
+  if (stages < producers) return false;
+  if (jobs_per_tile > 1) return true;
+  for (int m = 1; m * producers <= stages; ++m)
+    if ((stages - m * producers) % 2 == 0) return true;
+  return false;
+}
+
+constexpr int deepest_sound_ring(int fit, int producers, int jobs_per_tile) {
+  for (int st = fit; st >= 2; --st)
+    if (ring_waits_unambiguous(st, producers, jobs_per_tile)) return st;
+  return 0;
+}
+
+// IL: K pages in the interleaved layout (each token's 128 value bytes then its
+// 4 scale bytes), staged raw and rewritten into the MMA layout by the producers.
+template <int NEXT_N, int H, bool IL = false>
 struct Cfg {
   static constexpr int N = NEXT_N * H;
   static constexpr int NC = N <= 256 ? N : (N % 256 == 0 ? 256 : H);   // accumulator columns per job
@@ -100,12 +135,16 @@ struct Cfg {
   static constexpr int QBOX = N <= 256 ? N : (N % 256 == 0 ? 256 : 192);
   static constexpr int Q_BYTES = N * kHeadDim;
   static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(kTile, NC);
-  // K ring depth: as many 128-token stages as fit beside two Q slots (at most 8).
+  // K ring depth: as many 128-token stages as fit beside two Q slots (at
+  // most 8), with as many producer warps (3, else 2) as keep the ring's
+  // parity waits sound.
   static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64 +
-                               kCtxSmem * 4;
-  static constexpr int PER_STAGE = kStageBytes + kScaleSlot + 16 + 16;
-  static constexpr int STAGES = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
-  static_assert(STAGES >= 2, "shared memory");
+                               kCtxSmem * 4 + 16;
+  static constexpr int PER_STAGE = kStageBytes + kScaleSlot + 16 + 16 + (IL ? kStgBytes + 8 : 0);
+  static constexpr int FIT = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
+  static constexpr int PRODUCERS = ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2;
+  static constexpr int STAGES = deepest_sound_ring(FIT, PRODUCERS, C);
+  static_assert(STAGES >= 2 && ring_waits_unambiguous(STAGES, PRODUCERS, C), "shared memory");
   static_assert(N % QBOX == 0 && NC % 16 == 0 && NC <= 256 && ACC * NC <= 512, "shape");
 };
 
@@ -115,10 +154,10 @@ struct Part {        // this CTA's share of the work
 };
 
 struct SmemLayout {
-  uint32_t k, q, sc, meta, ids, bar, misc, ctx, total;
+  uint32_t k, q, sc, meta, ids, bar, misc, ctx, stg, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc, bool il) {
   SmemLayout L;
   L.k = 0;
   L.q = L.k + stages * kStageBytes;
@@ -126,9 +165,10 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int a
   L.meta = L.sc + stages * kScaleSlot;
   L.ids = L.meta + stages * 16;
   L.bar = L.ids + kProducers * kLookahead * 32 * 4;
-  L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1);
+  L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1 + (il ? stages : 0));
   L.ctx = L.misc + 64;
-  L.total = L.ctx + kCtxSmem * 4;
+  L.stg = (L.ctx + kCtxSmem * 4 + 15) / 16 * 16;      // raw interleaved pages, one tile per stage
+  L.total = L.stg + (il ? stages * kStgBytes : 0);
   return L;
 }
 
@@ -425,15 +465,16 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
   }
 }
 
-template <int NEXT_N, int H, bool FUSED>
+template <int NEXT_N, int H, bool FUSED, bool IL>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
                  const TcParams p) {
-  using K = Cfg<NEXT_N, H>;
+  using K = Cfg<NEXT_N, H, IL>;
+  constexpr int NP = K::PRODUCERS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int stages = K::STAGES;
-  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC);
+  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC, IL);
   const uint32_t s_base = ptx::smem_addr(smem);
   const uint32_t s_k = s_base + L.k, s_q = s_base + L.q;
   float* scales = reinterpret_cast<float*>(smem + L.sc);
@@ -447,6 +488,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   auto tfull = [&](int a) { return bar + 8u * (2 * stages + 4 + a); };
   auto tempty = [&](int a) { return bar + 8u * (2 * stages + 4 + K::ACC + a); };
   const uint32_t drain = bar + 8u * (2 * stages + 4 + 2 * K::ACC);
+  auto stgbar = [&](int s) { return bar + 8u * (2 * stages + 4 + 2 * K::ACC + 1 + s); };   // IL staging
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   int* fill_next = reinterpret_cast<int*>(smem + L.misc + 8);      // next -inf fill unit to take
@@ -460,7 +502,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   // ---- set-up --------------------------------------------------------------
   if (warp == 0) {
     if (lane == 0) {
-      ptx::prefetch_tensormap(&tmap_kv);
+      if constexpr (!IL) ptx::prefetch_tensormap(&tmap_kv);
       ptx::prefetch_tensormap(&tmap_q);
     }
     // The context lengths' lines are pulled into L2 first (a prefetch returns
@@ -487,6 +529,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         ptx::mbar_init(tempty(a), 4);
       }
       ptx::mbar_init(drain, 1);
+      if constexpr (IL)
+        for (int s = 0; s < stages; ++s) ptx::mbar_init(stgbar(s), 1);
       *abort_flag = 0;
       *fill_next = 0;
       *epi_done = 0;
@@ -510,8 +554,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     raise_status(p.status, SAI_STATUS_TIMEOUT);
   };
 
-  if (warp < kProducers) {
-    // ---- producers: warp pw issues tiles pw, pw + kProducers, ... ----------------
+  if (warp < NP) {
+    // ---- producers: warp pw issues tiles pw, pw + NP, ... ------------------------
     // A tile's copies go out as two warp instructions: lane l loads the values
     // of page l of the tile (a 128-byte swizzled tensor box), then its scales
     // (a contiguous bulk copy).
@@ -524,7 +568,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     const int tok_per_box = P >= kTile ? kTile : P;
     const uint32_t box_bytes = (uint32_t)tok_per_box * kTokenBytes;
     const int pl = lane;                                 // page of the tile this lane serves
-    const int own = pt.n_tiles > pw ? (pt.n_tiles - pw + kProducers - 1) / kProducers : 0;
+    const int own = pt.n_tiles > pw ? (pt.n_tiles - pw + NP - 1) / NP : 0;
     // Two cursors over this CTA's tiles: `cur` at this warp's tile being
     // issued, `la` kLookahead own tiles ahead, whose page ids are copied into a
     // shared-memory ring with cp.async so their latency overlaps the pipeline.
@@ -574,7 +618,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         const int32_t* src = p.block_table + (v ? (int64_t)la.b * p.bt_stride + (tok0 >> log2p) : 0);
         ptx::cp_async_4(ring + (uint32_t)(((la_j % kLookahead) * 32 + lane) * 4), src, v ? 4u : 0u);
         if (la_j + 1 < own)
-          for (int x = 0; x < kProducers; ++x) la.advance(p, cc_la, lane);
+          for (int x = 0; x < NP; ++x) la.advance(p, cc_la, lane);
         ++la_j;
       }
       ptx::cp_async_commit();
@@ -585,7 +629,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     bool ok = true;
     int j = 0;
     for (; j < own && ok; ++j) {
-      const int i = pw + j * kProducers;
+      const int i = pw + j * NP;
       const int s = i % stages;
       const uint32_t ph = (uint32_t)(i / stages) & 1u;
       const bool is_new = (i == 0) || (cur.t == 0);
@@ -601,44 +645,94 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const bool bad = need && (pg < 0 || pg >= p.num_pages);
       const bool load = need && !bad;
       const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
-      if (bad) {
-        for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
-        ptx::fence_proxy_async_smem();
-        raise_status(p.status, SAI_STATUS_BAD_PAGE);
-      }
-      if (lane == 0) {
-        meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
-                            (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes);
-      __syncwarp();
-      if (load) {
-        const int y = P > kTile ? (cur.t & 1) * kTile : 0;                       // half of a 256-token page
-        const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : pl * P * kHeadDim);
-        ptx::tma_load_3d(dst, &tmap_kv, 0, y, (int)pg, full(s), pol_k);
-        const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)P * kHeadDim + (int64_t)y * kScaleBytes;
-        const uint32_t sdst = s_base + L.sc + s * kScaleSlot + (P >= kTile ? 0 : pl * P * kScaleBytes);
-        ptx::bulk_load(sdst, src, (uint32_t)tok_per_box * kScaleBytes, full(s), pol_k);
+      if constexpr (IL) {
+        // The tile's pages as stored (P * 132 contiguous bytes, 16-byte
+        // aligned since P is a multiple of 4) come into the stage's staging
+        // slot with bulk copies, one lane per page; once they land, the warp
+        // rewrites them into the stage: values into the swizzled K-major
+        // layout, scales into token order.
+        if (bad) raise_status(p.status, SAI_STATUS_BAD_PAGE);
+        if (lane == 0) {
+          meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
+                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_expect_tx(stgbar(s), nload * box_bytes);
+        __syncwarp();
+        if (load) {
+          const int y = P > kTile ? (cur.t & 1) * kTile : 0;                     // half of a 256-token page
+          const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)y * kTokenBytes;
+          const uint32_t dst = s_base + L.stg + s * kStgBytes + (P >= kTile ? 0 : pl * box_bytes);
+          ptx::bulk_load(dst, src, box_bytes, stgbar(s), pol_k);
+        }
+        if (!ptx::mbar_wait_warp(stgbar(s), ph, abort_flag, kWaitBudget)) {
+          ok = false;
+          if (lane == 0) fail();
+          const int zero_flag = 0;
+          ptx::mbar_wait_warp(stgbar(s), ph, &zero_flag, 1LL << 26);       // the copies land before exit
+          break;
+        }
+        // Lane (c, r0): 16-byte value chunk c of tokens r0, r0 + 4, ...; the
+        // 132-byte token pitch makes the source words only 4-byte aligned and
+        // puts the 32 lanes' words in 32 distinct banks.
+        const uint8_t* stg = smem + L.stg + s * kStgBytes;
+        uint8_t* kst = smem + L.k + s * kStageBytes;
+        const int c = lane & 7;
+#pragma unroll 4
+        for (int m = 0; m < kTile / 4; ++m) {
+          const int r = (lane >> 3) + 4 * m;
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(stg + r * kTokenBytes + c * 16);
+          *reinterpret_cast<uint4*>(kst + r * kHeadDim + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        for (int r = lane; r < kTile; r += 32)
+          scales[s * kTile + r] = *reinterpret_cast<const float*>(stg + r * kTokenBytes + kHeadDim);
+        __syncwarp();
+        if (bad)
+          for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
+        ptx::fence_proxy_async_smem();                   // generic stores, then the MMA's async-proxy reads
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(full(s));
+      } else {
+        if (bad) {
+          for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
+          ptx::fence_proxy_async_smem();
+          raise_status(p.status, SAI_STATUS_BAD_PAGE);
+        }
+        if (lane == 0) {
+          meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
+                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes);
+        __syncwarp();
+        if (load) {
+          const int y = P > kTile ? (cur.t & 1) * kTile : 0;                       // half of a 256-token page
+          const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : pl * P * kHeadDim);
+          ptx::tma_load_3d(dst, &tmap_kv, 0, y, (int)pg, full(s), pol_k);
+          const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)P * kHeadDim + (int64_t)y * kScaleBytes;
+          const uint32_t sdst = s_base + L.sc + s * kScaleSlot + (P >= kTile ? 0 : pl * P * kScaleBytes);
+          ptx::bulk_load(sdst, src, (uint32_t)tok_per_box * kScaleBytes, full(s), pol_k);
+        }
       }
       __syncwarp();
       if (j == 0)
         for (int k = 1; k < kLookahead; ++k) issue_ids();     // the lookahead, after the first copies
       issue_ids();                                             // refill the slot just read
       if (j + 1 < own)
-        for (int x = 0; x < kProducers; ++x) step();
+        for (int x = 0; x < NP; ++x) step();
     }
     // Warp 0 still loads Q for requests that start in the other warps' last tiles.
     if (pw == 0 && ok && own > 0)
       while (ci + 1 < pt.n_tiles && qok) step();
     ok = ok && qok;
     ptx::cp_async_wait<0>();
-    if (!ok) {
-      // Let this warp's copies already issued land before the CTA exits.
+    if (!IL && !ok) {
+      // Let this warp's copies already issued land before the CTA exits (an
+      // interleaved tile's copies have always landed before its stage is full).
       const int zero_flag = 0;
-      const int i_end = pw + j * kProducers;
+      const int i_end = pw + j * NP;
       for (int k2 = max(0, i_end - stages); k2 < i_end; ++k2)
-        if (k2 % kProducers == pw)
+        if (k2 % NP == pw)
           ptx::mbar_wait_warp(full(k2 % stages), (uint32_t)(k2 / stages) & 1u, &zero_flag, 1LL << 26);
     }
   } else if (warp == kMmaWarp) {
@@ -685,7 +779,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kFirstEpiWarp) {   // (a producer warp left idle by Cfg::PRODUCERS goes on to the fill)
     // ---- epilogue ---------------------------------------------------------------
     const int ew = warp - kFirstEpiWarp;
     const int wg = ew >> 2;
@@ -893,14 +987,14 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-template <int NEXT_N, int H, bool FUSED>
+template <int NEXT_N, int H, bool FUSED, bool IL>
 cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
-  using K = Cfg<NEXT_N, H>;
+  using K = Cfg<NEXT_N, H, IL>;
   EncodeTiled enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const int P = a.page_size;
   CUtensorMap tkv, tq;
-  {
+  if (!IL) {   // the interleaved layout's pages are bulk copies, without a tensor map
     const uint64_t np = (uint64_t)(a.num_pages < (int64_t)INT32_MAX ? a.num_pages : (int64_t)INT32_MAX);
     const TmapKey key{a.kv, np, (uint32_t)P, 3};
     if (!tmap_lookup(key, &tkv)) {
@@ -929,12 +1023,14 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
       tmap_store(key, tq);
     }
   }
-  const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC);
+  if (IL) tkv = tq;                                      // never read
+  const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC, IL);
   const size_t smem = (size_t)L.total + 1024;
+  if (smem > (size_t)kMaxSmem) return cudaErrorInvalidConfiguration;
   static int smem_set[64] = {0};
-  static_assert(K::STAGES * kStageBytes + 2 * K::Q_BYTES >= (int)kSelectSmem + 1024 + 4 * 8192,
+  static_assert(!FUSED || K::STAGES * kStageBytes + 2 * K::Q_BYTES >= (int)kSelectSmem + 1024 + 4 * 8192,
                 "fused top-k scratch (and the keys of 8192-column rows) fit the drained K stages and Q slots");
-  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED>, smem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED, IL>, smem, smem_set);
   if (e != cudaSuccess) return e;
 
   TcParams p;
@@ -958,26 +1054,43 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H, FUSED>, tkv, tq, p);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H, FUSED, IL>, tkv, tq, p);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
 }  // namespace
 
+#ifndef SAI_LOGITS_INTERLEAVED
 cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream) {
   const bool fused = a.indices != nullptr;
   switch (a.next_n * 1000 + a.heads) {
-    case 1064: return fused ? launch_tc<1, 64, true>(a, stream) : launch_tc<1, 64, false>(a, stream);
-    case 2064: return fused ? launch_tc<2, 64, true>(a, stream) : launch_tc<2, 64, false>(a, stream);
-    case 3064: return fused ? launch_tc<3, 64, true>(a, stream) : launch_tc<3, 64, false>(a, stream);
-    case 4064: return fused ? launch_tc<4, 64, true>(a, stream) : launch_tc<4, 64, false>(a, stream);
-    case 1128: return fused ? launch_tc<1, 128, true>(a, stream) : launch_tc<1, 128, false>(a, stream);
-    case 2128: return fused ? launch_tc<2, 128, true>(a, stream) : launch_tc<2, 128, false>(a, stream);
-    case 3128: return fused ? launch_tc<3, 128, true>(a, stream) : launch_tc<3, 128, false>(a, stream);
-    case 4128: return fused ? launch_tc<4, 128, true>(a, stream) : launch_tc<4, 128, false>(a, stream);
+    case 1064: return fused ? launch_tc<1, 64, true, false>(a, stream) : launch_tc<1, 64, false, false>(a, stream);
+    case 2064: return fused ? launch_tc<2, 64, true, false>(a, stream) : launch_tc<2, 64, false, false>(a, stream);
+    case 3064: return fused ? launch_tc<3, 64, true, false>(a, stream) : launch_tc<3, 64, false, false>(a, stream);
+    case 4064: return fused ? launch_tc<4, 64, true, false>(a, stream) : launch_tc<4, 64, false, false>(a, stream);
+    case 1128: return fused ? launch_tc<1, 128, true, false>(a, stream) : launch_tc<1, 128, false, false>(a, stream);
+    case 2128: return fused ? launch_tc<2, 128, true, false>(a, stream) : launch_tc<2, 128, false, false>(a, stream);
+    case 3128: return fused ? launch_tc<3, 128, true, false>(a, stream) : launch_tc<3, 128, false, false>(a, stream);
+    case 4128: return fused ? launch_tc<4, 128, true, false>(a, stream) : launch_tc<4, 128, false, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
+#else
+cudaError_t launch_logits_tc_interleaved(const LogitsArgs& a, cudaStream_t stream) {
+  if (a.indices != nullptr) return cudaErrorInvalidValue;   // the fused launch reads page-split caches only
+  switch (a.next_n * 1000 + a.heads) {
+    case 1064: return launch_tc<1, 64, false, true>(a, stream);
+    case 2064: return launch_tc<2, 64, false, true>(a, stream);
+    case 3064: return launch_tc<3, 64, false, true>(a, stream);
+    case 4064: return launch_tc<4, 64, false, true>(a, stream);
+    case 1128: return launch_tc<1, 128, false, true>(a, stream);
+    case 2128: return launch_tc<2, 128, false, true>(a, stream);
+    case 3128: return launch_tc<3, 128, false, true>(a, stream);
+    case 4128: return launch_tc<4, 128, false, true>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+#endif
 
 }  // namespace sai
