@@ -141,9 +141,13 @@ SAI_API size_t sai_top_k_workspace_bytes(int32_t rows, int64_t max_len, int32_t 
  *                 receives, in entries [0, k), the column indices of its
  *                 min(k, n_r) largest logits, then -1 in every remaining entry
  *                 up to k.  If n_r <= k the indices are exactly 0 .. n_r - 1.
- *                 Entries are ordered by increasing column index among those
- *                 strictly greater than the k-th largest value, followed by
- *                 the ties at that value, lowest columns first.
+ *                 Of the columns tied at the k-th largest value, the lowest
+ *                 are taken.  Order (deterministic): the select reads the
+ *                 k-th largest key in radix digits of 8, 12 and 12 bits and
+ *                 stops at the first digit whose bin it takes whole (at the
+ *                 last digit the bin holds only ties); entries are the
+ *                 columns above that bin, ascending, then the columns taken
+ *                 from it, ascending.
  *   workspace     device, workspace_bytes >= sai_top_k_workspace_bytes(...);
  *                 may be null when that is 0.
  *

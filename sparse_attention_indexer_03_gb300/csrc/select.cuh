@@ -9,8 +9,10 @@
 // the lanes of one atomic never hit the same word or bank.  Passes 2 and 3
 // see only the keys of the chosen bin and use one plain 4096-bin histogram
 // each.  The select stops as soon as every key of the chosen bin is taken.
-// Output order is deterministic: the columns strictly above the threshold,
-// ascending, then the ties at the threshold, lowest columns first.
+// Output order is deterministic: the columns above the last bin the select
+// examined, ascending, then the columns taken from that bin, ascending (the
+// whole bin when the select stopped early; otherwise the bin is the ties at
+// the k-th largest key, and the lowest of them are taken).
 #pragma once
 
 #include "common.cuh"
@@ -45,15 +47,25 @@ struct SelectShared {
   uint32_t digit, remaining, bin_count;
 };
 
+// A group that holds all of its row: its own histogram counts are the row's.
+struct LocalCounts {
+  template <int MP>
+  __device__ __forceinline__ void operator()(int, uint32_t (&)[MP], int, int, int) const {}
+};
+
 // Radix select over the keys each thread visits through `for_each(f)`, which
 // calls f(valid, key) for each of the thread's keys.  The counting adds are
 // predicated instructions, so the loops carry no data-dependent branch.
 // `tid` is the thread's
 // index in the group (0 .. NT-1, whole warps), `bar()` a barrier of the group,
 // `hist` kSelectSmem bytes of shared memory.  Three barriers per pass.
-template <int NT, typename Bar, typename ForEach>
+// `row_counts(pass, cnt, per, wbase, lane)` turns the counts of the bins a
+// thread owns (bin wbase + 32 * i + lane in cnt[i], i < per) into the whole
+// row's, for rows split over several groups; every group then takes the
+// same digits.
+template <int NT, typename Bar, typename ForEach, typename RowCounts = LocalCounts>
 __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint32_t* hist, uint32_t k, int tid,
-                                                     Bar bar, ForEach for_each) {
+                                                     Bar bar, ForEach for_each, RowCounts row_counts = {}) {
   constexpr int kW = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* h1 = hist;                              // pass 1: [bin][lane]; pass 3: plain, reused
@@ -92,12 +104,12 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
     };
     constexpr int kMaxPer = (kSelBins2 + NT - 1) / NT;
     uint32_t cnt[kMaxPer];
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) cnt[i] = i < per ? count(wbase + 32 * i + lane) : 0u;
+    row_counts(pass, cnt, per, wbase, lane);
     uint32_t mine = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxPer; ++i) {
-      cnt[i] = i < per ? count(wbase + 32 * i + lane) : 0u;
-      mine += cnt[i];
-    }
+    for (int i = 0; i < kMaxPer; ++i) mine += cnt[i];
     const uint32_t wsum = __reduce_add_sync(0xffffffffu, mine);
     if (lane == 0) sh.wtot[warp] = wsum;
     bar();
@@ -187,16 +199,27 @@ __device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const Selec
   bar();                                            // warp_gt / warp_eq free for the next row
 }
 
+// A group that holds all of its row: nothing precedes it.
+struct FirstGroup {
+  template <int NT>
+  __device__ __forceinline__ void operator()(const SelectShared<NT>&, uint32_t&, uint32_t&) const {}
+};
+
 // Ordered compaction by lanes.  Lane l of warp w owns the run of columns
-// [base, base + len) with base = w * 32 * len + l * len, so column order is
+// [base, base + len) with base = w * 32 * len + l * len (plus the group's
+// first column), so column order is
 // (warp, lane, slot): each lane counts its own selected keys, one packed
 // warp scan gives every lane its offset, one barrier gives every warp its
 // offset, and each lane then writes its keys in order with no warp-wide
 // operation per key.  `key_at.for_each(f)` calls f(i, key) for the keys of
-// columns base + i; only i < len and columns below n count.
-template <int NT, typename Bar, typename KeyAt>
+// columns base + i; only i < len and columns below n count.  For a row split
+// over groups, `preceding(sh, pg, pe)` adds to a thread's offsets the keys
+// above and at the threshold that the groups holding earlier columns select
+// (sh.warp_gt / warp_eq hold this group's per-warp counts when it is called).
+template <int NT, typename Bar, typename KeyAt, typename Preceding = FirstGroup>
 __device__ __forceinline__ void compact_lanes(SelectShared<NT>& sh, const SelectResult& s, int n, int k,
-                                              int32_t* out, int tid, Bar bar, int base, int len, KeyAt key_at) {
+                                              int32_t* out, int tid, Bar bar, int base, int len, KeyAt key_at,
+                                              Preceding preceding = {}) {
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t n_gt = (uint32_t)k - s.remaining;
   uint32_t cg = 0, ce = 0;
@@ -220,6 +243,7 @@ __device__ __forceinline__ void compact_lanes(SelectShared<NT>& sh, const Select
   const uint32_t excl = incl - x;
   uint32_t pg = excl >> 16, pe = excl & 0xffffu;
   for (int w = 0; w < warp; ++w) { pg += sh.warp_gt[w]; pe += sh.warp_eq[w]; }
+  preceding(sh, pg, pe);
   key_at.for_each([&](int i, uint32_t key) {
     const uint32_t m = key & s.mask;
     const int c = base + i;

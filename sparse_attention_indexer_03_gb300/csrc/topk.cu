@@ -2,9 +2,9 @@
 // the logits launch in aiter PR 4244, opening paragraph).
 //
 // One CTA of 1024 threads per row runs the exact radix select of select.cuh
-// and writes the row's indices in a deterministic order: the columns strictly
-// above the threshold, ascending, then the ties at the threshold, lowest
-// columns first.  Rows of a logical width up to 16384 are held in registers
+// and writes the row's indices in a deterministic order: the columns above
+// the last bin the select examined, ascending, then the columns taken from
+// that bin, ascending (ties at the k-th largest value: the lowest columns).  Rows of a logical width up to 16384 are held in registers
 // (each thread a run of KPT consecutive columns, read from global memory
 // once); wider rows up to 40960 long are copied into shared memory once their
 // length is known, and longer ones re-read from global memory (mostly L2) on
@@ -15,6 +15,12 @@
 // and waits for it to complete before reading any logits.  It then lets its
 // own dependents start at once: with one CTA per row, a decode batch leaves
 // most SMs free, where the next launch can run its set-up.
+//
+// Few long rows (up to 131072 columns, too few rows to fill the GPU one CTA
+// each) are split over a thread-block cluster of 2 to 8 CTAs, each holding
+// 16384 columns in registers: each radix pass adds the CTAs' histograms
+// through distributed shared memory, so every CTA takes the same digits, and
+// the compaction offsets each CTA by the keys its predecessors select.
 #include <algorithm>
 
 #include "common.cuh"
@@ -25,7 +31,6 @@ namespace sai {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ int64_t row_len(const TopKArgs& a, int64_t r) {
   const int b = (int)(r / a.next_n), j = (int)(r % a.next_n);
@@ -39,6 +44,26 @@ __device__ __forceinline__ void write_short_row(int32_t* out, int64_t n, int k) 
 struct CtaBar {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
+
+// Keys of columns [base, base + KPT) of a row (0 past the width).  A 16-byte
+// aligned row is read as float4 vectors: a quarter of the load instructions
+// of scalar reads, whose lanes, KPT words apart, each touch their own sector.
+template <int KPT>
+__device__ __forceinline__ void load_run(const float* row, int base, int64_t width, uint32_t (&key)[KPT]) {
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && base + KPT <= width) {
+#pragma unroll
+    for (int v = 0; v < KPT / 4; ++v) {
+      const float4 x = *reinterpret_cast<const float4*>(row + base + 4 * v);
+      key[4 * v] = float_key(x.x);
+      key[4 * v + 1] = float_key(x.y);
+      key[4 * v + 2] = float_key(x.z);
+      key[4 * v + 3] = float_key(x.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) key[i] = base + i < width ? float_key(row[base + i]) : 0u;
+  }
+}
 
 // ---- rows held in registers: lane l of warp w holds the KPT columns from
 // w * 32 * KPT + l * KPT on, key[i] the i-th of them ---------------------------
@@ -56,11 +81,7 @@ topk_reg_kernel(TopKArgs a) {
   // The keys are read before the row's length is known (columns below W
   // always exist), so the two loads overlap.
   uint32_t key[KPT];
-#pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    const int c = base + i;
-    key[i] = c < a.width ? float_key(row[c]) : 0u;
-  }
+  load_run<KPT>(row, base, a.width, key);
   const int64_t n64 = row_len(a, r);
   int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
   const int k = a.k;
@@ -78,6 +99,108 @@ topk_reg_kernel(TopKArgs a) {
   };
   const SelectResult s = radix_select<kThreads>(sh, hist_smem, (uint32_t)k, tid, CtaBar{}, for_each);
   compact_lanes<kThreads>(sh, s, n, k, out, tid, CtaBar{}, base, KPT, RegRun<KPT>{key, KPT});
+}
+
+// ---- few long rows: CTA `rank` of a cluster of CL holds columns
+// [rank * 16384, (rank + 1) * 16384) of the row, in registers as above --------
+constexpr int kClusterKpt = 16;
+constexpr int kClusterSlice = kClusterKpt * kThreads;     // 16384 columns per CTA
+
+// Histogram counts of the whole row: each CTA publishes the counts of the
+// bins its threads own in one of two exchange arrays (alternating passes, so
+// a pass never overwrites an array another CTA may still be reading), and
+// each thread sums its bins over the cluster.
+template <int CL>
+struct ClusterCounts {
+  uint32_t* xch;                                           // 2 * kSelBins2 words
+  template <int MP>
+  __device__ __forceinline__ void operator()(int pass, uint32_t (&cnt)[MP], int per, int wbase, int lane) const {
+    uint32_t* x = xch + (pass & 1) * kSelBins2;
+#pragma unroll
+    for (int i = 0; i < MP; ++i)
+      if (i < per) x[wbase + 32 * i + lane] = cnt[i];
+    ptx::cluster_sync();
+#pragma unroll
+    for (int i = 0; i < MP; ++i)
+      if (i < per) {
+        uint32_t v[CL];                                    // all CL loads in flight, then the sum
+#pragma unroll
+        for (int c = 0; c < CL; ++c) v[c] = ptx::ld_cluster_u32(x + wbase + 32 * i + lane, (uint32_t)c);
+        uint32_t t = 0;
+#pragma unroll
+        for (int c = 0; c < CL; ++c) t += v[c];
+        cnt[i] = t;
+      }
+  }
+};
+
+// Keys above and at the threshold selected by the CTAs of lower rank (which
+// hold the earlier columns).  The second barrier keeps every CTA's shared
+// memory alive until all the cluster's reads of it are done.
+template <int CL>
+struct ClusterPreceding {
+  uint32_t* totals;                                        // 2 words
+  uint32_t rank;
+  template <int NT>
+  __device__ __forceinline__ void operator()(const SelectShared<NT>& sh, uint32_t& pg, uint32_t& pe) const {
+    if (threadIdx.x == 0) {
+      uint32_t tg = 0, te = 0;
+      for (int w = 0; w < NT / 32; ++w) { tg += sh.warp_gt[w]; te += sh.warp_eq[w]; }
+      totals[0] = tg;
+      totals[1] = te;
+    }
+    __syncwarp();                                          // the barrier is warp-aligned
+    ptx::cluster_sync();
+    uint32_t vg[CL], ve[CL];                               // all loads in flight, then the sums
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      vg[c] = (uint32_t)c < rank ? ptx::ld_cluster_u32(totals, (uint32_t)c) : 0u;
+      ve[c] = (uint32_t)c < rank ? ptx::ld_cluster_u32(totals + 1, (uint32_t)c) : 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < CL; ++c) { pg += vg[c]; pe += ve[c]; }
+    ptx::cluster_sync();
+  }
+};
+
+template <int CL>
+__global__ void __launch_bounds__(kThreads)
+topk_cluster_kernel(TopKArgs a) {
+  constexpr int KPT = kClusterKpt, kSlice = kClusterSlice;
+  extern __shared__ uint32_t hist_smem[];
+  __shared__ SelectShared<kThreads> sh;
+  __shared__ uint32_t xch[2 * kSelBins2];
+  __shared__ uint32_t totals[2];
+  ptx::wait_prerequisites();
+  ptx::launch_dependents();
+  const int tid = threadIdx.x;
+  const uint32_t rank = ptx::cluster_rank();
+  const int64_t r = blockIdx.x / CL;
+  const float* row = a.logits + r * a.stride;              // 64-bit row base
+  const int base = (int)rank * kSlice + tid * KPT;
+  uint32_t key[KPT];
+  load_run<KPT>(row, base, a.width, key);
+  const int64_t n64 = row_len(a, r);
+  int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
+  const int k = a.k;
+  if (n64 <= k) {                                          // the same for every CTA of the cluster
+    if (rank == 0) write_short_row(out, n64, k);
+    return;
+  }
+  const int n = (int)n64;                                  // <= CL * kSlice
+  const bool warp_live = (int)rank * kSlice + (tid >> 5) * 32 * KPT < n;   // warp-uniform
+  auto for_each = [&](auto&& f) {
+    if (warp_live) {
+#pragma unroll
+      for (int i = 0; i < KPT; ++i) f(base + i < n, key[i]);
+    }
+  };
+  // Every CTA of the cluster runs the same passes (the digits come from the
+  // cluster's counts) and so the same cluster barriers.
+  const SelectResult s =
+      radix_select<kThreads>(sh, hist_smem, (uint32_t)k, tid, CtaBar{}, for_each, ClusterCounts<CL>{xch});
+  compact_lanes<kThreads>(sh, s, n, k, out, tid, CtaBar{}, base, KPT, RegRun<KPT>{key, KPT},
+                          ClusterPreceding<CL>{totals, rank});
 }
 
 // ---- wider rows: a row of up to kSmemKeys columns has its keys copied into
@@ -112,7 +235,7 @@ topk_smem_kernel(TopKArgs a) {
 
 template <typename Kern>
 cudaError_t launch_pdl(Kern kern, unsigned grid, const TopKArgs& a, cudaStream_t stream, int* smem_set,
-                       size_t smem, size_t smem_max) {
+                       size_t smem, size_t smem_max, unsigned cluster = 1) {
   cudaError_t e = ensure_dynamic_smem(kern, smem_max, smem_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -120,11 +243,15 @@ cudaError_t launch_pdl(Kern kern, unsigned grid, const TopKArgs& a, cudaStream_t
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
@@ -136,9 +263,22 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.batch * a.next_n;
   if (rows == 0) return cudaSuccess;
   const unsigned g = (unsigned)rows;
-  static int set4[64], set8[64], set16[64], set_smem[64];
+  static int set4[64], set8[64], set16[64], set_smem[64], set_c2[64], set_c4[64], set_c8[64];
+  // Rows wider than one CTA's registers go to a cluster (16384 columns per
+  // CTA) while the grid stays within four CTAs per SM; more rows fill the
+  // GPU one CTA each.  (Clusters of 16 CTAs of 8192 columns were slower on a
+  // single 131072-column row: 37 us against 30 us.)
+  const int sms = device_sm_count();
+  const int64_t slices = (a.width + kClusterSlice - 1) / kClusterSlice;
+  const int cl = slices <= 2 ? 2 : (slices <= 4 ? 4 : 8);
+  const bool clustered = a.width > kClusterSlice && slices <= 8 && rows * cl <= 4 * (int64_t)(sms > 0 ? sms : 152);
   cudaError_t e;
-  if (a.width <= 4 * kThreads) e = launch_pdl(topk_reg_kernel<4>, g, a, stream, set4, kSelectSmem, kSelectSmem);
+  if (clustered) {
+    const unsigned gc = (unsigned)(rows * cl);
+    if (cl == 2) e = launch_pdl(topk_cluster_kernel<2>, gc, a, stream, set_c2, kSelectSmem, kSelectSmem, 2);
+    else if (cl == 4) e = launch_pdl(topk_cluster_kernel<4>, gc, a, stream, set_c4, kSelectSmem, kSelectSmem, 4);
+    else e = launch_pdl(topk_cluster_kernel<8>, gc, a, stream, set_c8, kSelectSmem, kSelectSmem, 8);
+  } else if (a.width <= 4 * kThreads) e = launch_pdl(topk_reg_kernel<4>, g, a, stream, set4, kSelectSmem, kSelectSmem);
   else if (a.width <= 8 * kThreads) e = launch_pdl(topk_reg_kernel<8>, g, a, stream, set8, kSelectSmem, kSelectSmem);
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
   else e = launch_pdl(topk_smem_kernel, g, a, stream, set_smem,

@@ -98,3 +98,46 @@ def test_long_rows(W):
     got = _run_on_values(vals, ctx, next_n, k, W, stride=W + 5)
     n_r = np.clip(np.repeat(ctx, next_n) - next_n + np.tile(np.arange(next_n), 3) + 1, 0, W)
     assert_topk_exact(got, vals, n_r, k)
+
+
+def _ties_order(v: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Expected entries of a row whose values near the k-th largest are exact
+    ties: the columns above the k-th largest value ascending, then the lowest
+    columns equal to it."""
+    v = v[:n]
+    if n <= k:
+        return np.concatenate([np.arange(n), np.full(k - n, -1)])
+    thr = np.sort(v)[::-1][k - 1]
+    gt = np.flatnonzero(v > thr)
+    eq = np.flatnonzero(v == thr)[:k - len(gt)]
+    return np.concatenate([gt, eq])
+
+
+@pytest.mark.parametrize("W", [20000, 65536, 131072])
+def test_rows_split_over_a_cluster_match_one_cta_per_row(W):
+    # Few rows wider than 16384 columns are split over a cluster of 2, 4 or 8
+    # CTAs, 16384 columns each, while rows * cluster stays within four CTAs
+    # per SM; more rows take one CTA each.  The selection and its order must
+    # not depend on where the slices end: checked against the oracle's sets,
+    # against the tie order on rows of exact ties, and entry for entry
+    # against the same rows repeated until the launch takes one CTA per row.
+    rng = np.random.default_rng(W + 1)
+    k = 2048
+    vals = np.full((5, W), -1.0, np.float32)
+    vals[0, ::37] = 1.0
+    vals[1, ::29] = 1.0
+    vals[1, np.sort(rng.choice(W, 1000, replace=False))] = 2.0
+    vals[2] = rng.standard_normal(W).astype(np.float32)
+    vals[3] = rng.standard_normal(W).astype(np.float32)
+    vals[4, ::5] = 3.0
+    ctx = np.array([W, W, W, 1000, W - 16384 + 5])
+    got = _run_on_values(vals, ctx, 1, k, W)
+    assert_topk_exact(got, vals, ctx, k)
+    for i in (0, 1, 3, 4):
+        assert got[i].tolist() == _ties_order(vals[i], int(ctx[i]), k).tolist(), f"row {i}"
+    cl = 2 if W <= 2 * 16384 else (4 if W <= 4 * 16384 else 8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows in (4 * sms // cl - 4, 4 * sms // cl + 1):     # the largest clustered launch; one CTA per row
+        reps = -(-rows // 5)
+        again = _run_on_values(np.tile(vals, (reps, 1)), np.tile(ctx, reps), 1, k, W)
+        assert (again == np.tile(got, (reps, 1))).all(), rows
