@@ -24,8 +24,8 @@
 //              Interleaved caches (IL; each token's 128 value bytes, then its
 //              4 scale bytes, as the aiter PR 4244 reproducer builds them):
 //              the 132-byte token pitch is no tensor-map stride, so a lane
-//              bulk-copies its page as stored into a staging slot, and once
-//              the tile has landed the warp rewrites it into the stage layout
+//              bulk-copies its page as stored into the stage, and once the
+//              tile has landed the warp rewrites it in place into the layout
 //              above; the MMA and the epilogue are the same.
 //   warp 3     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
 //              A = the K stage (128 tokens x 128 B, K-major, 128-byte
@@ -96,7 +96,10 @@ struct TcParams {
 // shared memory by the partition, so the walks over requests read them there.
 constexpr int kCtxSmem = 512;
 
-constexpr int kStgBytes = kTile * kTokenBytes;   // one tile of interleaved pages as stored: 16,896 B
+// An interleaved stage: a tile of tokens as stored (128 * 132 = 16,896 B),
+// rewritten in place into the 16 KB MMA layout; rounded to 1 KB so every
+// stage base keeps the 128-byte swizzle's 1024-byte alignment.
+constexpr int kStageBytesIl = (kTile * kTokenBytes + 1023) / 1024 * 1024;
 
 // The producers wait for a stage's release by phase parity, which cannot tell
 // the release of the stage's use u - 1 from that of use u - 2: the wait is
@@ -123,7 +126,8 @@ constexpr int deepest_sound_ring(int fit, int producers, int jobs_per_tile) {
 }
 
 // IL: K pages in the interleaved layout (each token's 128 value bytes then its
-// 4 scale bytes), staged raw and rewritten into the MMA layout by the producers.
+// 4 scale bytes), copied into the stage as stored and rewritten there into the
+// MMA layout by the producers.
 template <int NEXT_N, int H, bool IL = false>
 struct Cfg {
   static constexpr int N = NEXT_N * H;
@@ -139,8 +143,9 @@ struct Cfg {
   // most 8), with as many producer warps (3, else 2) as keep the ring's
   // parity waits sound.
   static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64 +
-                               kCtxSmem * 4 + 16;
-  static constexpr int PER_STAGE = kStageBytes + kScaleSlot + 16 + 16 + (IL ? kStgBytes + 8 : 0);
+                               kCtxSmem * 4;
+  static constexpr int STAGE_BYTES = IL ? kStageBytesIl : kStageBytes;
+  static constexpr int PER_STAGE = STAGE_BYTES + kScaleSlot + 16 + 16 + (IL ? 8 : 0);
   static constexpr int FIT = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
   static constexpr int PRODUCERS = ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2;
   static constexpr int STAGES = deepest_sound_ring(FIT, PRODUCERS, C);
@@ -154,21 +159,20 @@ struct Part {        // this CTA's share of the work
 };
 
 struct SmemLayout {
-  uint32_t k, q, sc, meta, ids, bar, misc, ctx, stg, total;
+  uint32_t k, q, sc, meta, ids, bar, misc, ctx, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc, bool il) {
   SmemLayout L;
   L.k = 0;
-  L.q = L.k + stages * kStageBytes;
+  L.q = L.k + stages * (il ? kStageBytesIl : kStageBytes);
   L.sc = L.q + 2 * q_bytes;
   L.meta = L.sc + stages * kScaleSlot;
   L.ids = L.meta + stages * 16;
   L.bar = L.ids + kProducers * kLookahead * 32 * 4;
   L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1 + (il ? stages : 0));
   L.ctx = L.misc + 64;
-  L.stg = (L.ctx + kCtxSmem * 4 + 15) / 16 * 16;      // raw interleaved pages, one tile per stage
-  L.total = L.stg + (il ? stages * kStgBytes : 0);
+  L.total = L.ctx + kCtxSmem * 4;
   return L;
 }
 
@@ -623,6 +627,61 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
       ptx::cp_async_commit();
     };
+    // Interleaved tiles: once a tile's pages have landed in its stage as
+    // stored, the warp rewrites them in place (values into the swizzled
+    // K-major layout, scales into token order), then marks the stage full.
+    // Lane (c, r0) moves 16-byte value chunk c of tokens r0, r0 + 4, ...:
+    // the 132-byte token pitch leaves the source words 4-byte aligned and
+    // puts the 32 lanes' words in 32 distinct banks.
+    auto finish_il = [&](int fs, uint32_t fph, bool fbad) -> bool {
+      if (!ptx::mbar_wait_warp(stgbar(fs), fph, abort_flag, kWaitBudget)) {
+        if (lane == 0) fail();
+        const int zero_flag = 0;
+        ptx::mbar_wait_warp(stgbar(fs), fph, &zero_flag, 1LL << 26);    // the copies land before exit
+        return false;
+      }
+      // Token r's rewritten row [128 r, 128 r + 128) overlaps the stored
+      // bytes of tokens <= r only, so the warp rewrites 16 tokens at a time
+      // in increasing order, reading all 16 (values and scales) before
+      // writing any.
+      uint8_t* st = smem + L.k + fs * K::STAGE_BYTES;
+      const int c = lane & 7;
+#pragma unroll 1
+      for (int m = 0; m < kTile / 16; ++m) {
+        uint4 v[4];
+        float sv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = (lane >> 3) + 4 * u + 16 * m;
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(st + r * kTokenBytes + c * 16);
+          v[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          sv[u] = c == 0 ? *reinterpret_cast<const float*>(st + r * kTokenBytes + kHeadDim) : 0.f;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = (lane >> 3) + 4 * u + 16 * m;
+          *reinterpret_cast<uint4*>(st + r * kHeadDim + ((c ^ (r & 7)) << 4)) = v[u];
+          if (c == 0) scales[fs * kTile + r] = sv[u];
+        }
+      }
+      __syncwarp();
+      if (fbad)
+        for (int x = 0; x < tok_per_box; ++x) scales[fs * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
+      ptx::fence_proxy_async_smem();                   // generic stores, then the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(full(fs));
+      return true;
+    };
+    // Warps other than 0 issue their next tile's copies before rewriting the
+    // current tile, so two of their tiles are in flight.  Holding tile i
+    // while waiting for the release of tile i + NP - stages is deadlock-free
+    // when stages > NP: that release needs only earlier tiles.  Warp 0 does
+    // not hold: its Q loads wait for releases that may need its own tile.
+    const bool hold = IL && stages > NP && pw != 0;
+    int held_s = -1;                                   // stage of the held tile, -1 if none
+    uint32_t held_ph = 0;
+    bool held_bad = false;
     // Only the first tile's page ids go out before its K copies; the rest of
     // the lookahead follows them, off the first tile's latency chain.
     issue_ids();
@@ -647,10 +706,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const uint32_t nload = __popc(__ballot_sync(0xffffffffu, load));
       if constexpr (IL) {
         // The tile's pages as stored (P * 132 contiguous bytes, 16-byte
-        // aligned since P is a multiple of 4) come into the stage's staging
-        // slot with bulk copies, one lane per page; once they land, the warp
-        // rewrites them into the stage: values into the swizzled K-major
-        // layout, scales into token order.
+        // aligned since P is a multiple of 4) come into the stage with bulk
+        // copies, one lane per page; finish_il rewrites them in place.
         if (bad) raise_status(p.status, SAI_STATUS_BAD_PAGE);
         if (lane == 0) {
           meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
@@ -662,36 +719,21 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         if (load) {
           const int y = P > kTile ? (cur.t & 1) * kTile : 0;                     // half of a 256-token page
           const uint8_t* src = p.kv + pg * (int64_t)P * kTokenBytes + (int64_t)y * kTokenBytes;
-          const uint32_t dst = s_base + L.stg + s * kStgBytes + (P >= kTile ? 0 : pl * box_bytes);
+          const uint32_t dst = s_k + s * K::STAGE_BYTES + (P >= kTile ? 0 : pl * box_bytes);
           ptx::bulk_load(dst, src, box_bytes, stgbar(s), pol_k);
         }
-        if (!ptx::mbar_wait_warp(stgbar(s), ph, abort_flag, kWaitBudget)) {
+        if (hold) {                                    // rewrite the previous tile while this one lands
+          const int prev_s = held_s;
+          const uint32_t prev_ph = held_ph;
+          const bool prev_bad = held_bad;
+          held_s = s;                                  // (so an exit below still drains its copies)
+          held_ph = ph;
+          held_bad = bad;
+          if (prev_s >= 0 && !finish_il(prev_s, prev_ph, prev_bad)) { ok = false; break; }
+        } else if (!finish_il(s, ph, bad)) {
           ok = false;
-          if (lane == 0) fail();
-          const int zero_flag = 0;
-          ptx::mbar_wait_warp(stgbar(s), ph, &zero_flag, 1LL << 26);       // the copies land before exit
           break;
         }
-        // Lane (c, r0): 16-byte value chunk c of tokens r0, r0 + 4, ...; the
-        // 132-byte token pitch makes the source words only 4-byte aligned and
-        // puts the 32 lanes' words in 32 distinct banks.
-        const uint8_t* stg = smem + L.stg + s * kStgBytes;
-        uint8_t* kst = smem + L.k + s * kStageBytes;
-        const int c = lane & 7;
-#pragma unroll 4
-        for (int m = 0; m < kTile / 4; ++m) {
-          const int r = (lane >> 3) + 4 * m;
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(stg + r * kTokenBytes + c * 16);
-          *reinterpret_cast<uint4*>(kst + r * kHeadDim + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        for (int r = lane; r < kTile; r += 32)
-          scales[s * kTile + r] = *reinterpret_cast<const float*>(stg + r * kTokenBytes + kHeadDim);
-        __syncwarp();
-        if (bad)
-          for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
-        ptx::fence_proxy_async_smem();                   // generic stores, then the MMA's async-proxy reads
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(full(s));
       } else {
         if (bad) {
           for (int x = 0; x < tok_per_box; ++x) scales[s * kTile + (P >= kTile ? 0 : pl * P) + x] = __int_as_float(0x7fc00000);
@@ -720,6 +762,14 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       issue_ids();                                             // refill the slot just read
       if (j + 1 < own)
         for (int x = 0; x < NP; ++x) step();
+    }
+    if (held_s >= 0) {
+      if (ok) {
+        ok = finish_il(held_s, held_ph, held_bad);
+      } else {
+        const int zero_flag = 0;
+        ptx::mbar_wait_warp(stgbar(held_s), held_ph, &zero_flag, 1LL << 26);   // its copies land before exit
+      }
     }
     // Warp 0 still loads Q for requests that start in the other warps' last tiles.
     if (pw == 0 && ok && own > 0)
@@ -758,7 +808,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           if (!ptx::mbar_wait(tempty(a), ((uint32_t)(acc_count / K::ACC) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t d = tmem_base + (uint32_t)(a * K::NC);
-          const uint64_t adesc = ptx::desc_kmajor_sw128(s_k + s * kStageBytes);
+          const uint64_t adesc = ptx::desc_kmajor_sw128(s_k + s * K::STAGE_BYTES);
           const uint64_t bdesc = ptx::desc_kmajor_sw128(s_q + qs * K::Q_BYTES + c * K::NC * kHeadDim);
 #pragma unroll
           for (int k = 0; k < kHeadDim / 32; ++k)       // 32 bytes of K per instruction: +2 in 16-byte units
