@@ -871,6 +871,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
 #pragma unroll
           for (int x = 0; x < 16; ++x) w4[x] = (jr == 0 && h0 == 0 && x < 8) ? wn[x] : __ldg(wrow + (h0 >> 2) + x);
           ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(v);
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             float2* q = part + 2 * (x & 1);

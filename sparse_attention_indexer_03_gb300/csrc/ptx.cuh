@@ -246,6 +246,15 @@ __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t (&v)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Ties registers written by tcgen05.ld to this point (after the wait): the
+// load's outputs are defined at the load instruction as far as the compiler
+// knows, so without it a use could be scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(v[i]));
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored as rows of
 // 128 bytes with the 128-byte swizzle (8-row, 1024-byte atoms, atoms 1024
 // bytes apart along M/N).  Fields: start address >> 4 (bits 0-13), leading
