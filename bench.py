@@ -498,6 +498,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "path": ("one fused launch (logits, then top-k by the CTA completing each request)"
                                 if fused else "two launches (logits, top-k)"),
                        "logits_ms": lg_ms, "topk_ms": None if fused else tk_ms,
+                       "logits_ms_median": float(np.median(logits_ms)),
+                       "topk_ms_median": None if fused else float(np.median(topk_ms)),
                        "topk_gbs": None if fused else topk_bytes(w) / (tk_ms * 1e-3) / 1e9,
                        "parallelism": f"replicas x{world} (independent requests per GPU)"},
             "roofline": roof,
