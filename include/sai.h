@@ -302,6 +302,26 @@ SAI_API int sai_gather_selected_kv(const int32_t* indices, int64_t indices_strid
                            int32_t page_size, const uint8_t* kv_pool, int64_t num_pages, int32_t row_bytes,
                            int64_t* row_ids, uint8_t* out, uint32_t* status, sai_stream_t stream);
 
+/*
+ * sai_selftest_bounded_wait -- exercises the bounded wait that every pipeline
+ * wait of the library's kernels uses (one launch of one CTA).  The pages have
+ * no counterpart: a correct pipeline never lets a wait run out, so this entry
+ * point builds the one situation that does, a shared-memory barrier that
+ * nothing ever arrives on, to check that the wait ends, reports
+ * SAI_STATUS_TIMEOUT and leaves the context usable.
+ *
+ *   mode     0: the wait's cycle budget is `cycles`;
+ *            1: the wait has the kernels' budget (2^31 SM cycles, about 1 s)
+ *               and a second warp raises the CTA's abort flag after `cycles`
+ *               cycles, as a failing warp does in the kernels.
+ *   cycles   1 .. 2^31 SM clock cycles.
+ *   status   device uint32 word (required); SAI_STATUS_TIMEOUT is OR-ed in
+ *            when the wait gives up, which it always does.
+ * Returns SAI_ERR_INVALID_ARGUMENT for another mode, a cycle count out of
+ * range or a null status.
+ */
+SAI_API int sai_selftest_bounded_wait(int32_t mode, int64_t cycles, uint32_t* status, sai_stream_t stream);
+
 /* Static, human-readable name of a return code. */
 SAI_API const char* sai_error_string(int code);
 

@@ -80,6 +80,7 @@ _SIGS = {
                                               _c.c_int32, _P, _P]),
     "sai_gather_selected_kv": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _P, _c.c_int64,
                                           _c.c_int32, _P, _c.c_int64, _c.c_int32, _P, _P, _P, _P]),
+    "sai_selftest_bounded_wait": (_c.c_int, [_c.c_int32, _c.c_int64, _P, _P]),
     "sai_error_string": (_c.c_char_p, [_c.c_int]),
     "sai_version": (_c.c_int, []),
 }
@@ -302,6 +303,18 @@ def gather_selected_kv(indices, next_n: int, block_table, page_size: int, kv_poo
         _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_gather_selected_kv")
+
+
+def selftest_bounded_wait(mode: int, cycles: int, status, *, stream=None) -> None:
+    """Run the bounded-wait self-test (see `sai_selftest_bounded_wait`):
+    mode 0 lets the budget of `cycles` run out, mode 1 raises the abort flag
+    after `cycles`; either way SAI_STATUS_TIMEOUT is OR-ed into `status`."""
+    import torch
+
+    code = library().sai_selftest_bounded_wait(int(mode), int(cycles), _ptr(status, torch.int32, "status"),
+                                               _stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_selftest_bounded_wait")
 
 
 def top_k_workspace_bytes(rows: int, max_len: int, k: int) -> int:

@@ -37,6 +37,14 @@ extern "C" {
 
 int sai_version(void) { return 100; }
 
+int sai_selftest_bounded_wait(int32_t mode, int64_t cycles, uint32_t* status, sai_stream_t stream) {
+  if ((mode != 0 && mode != 1) || cycles < 1 || cycles > (int64_t{1} << 31) || status == nullptr)
+    return SAI_ERR_INVALID_ARGUMENT;
+  if (!sai::aligned(status, 4)) return SAI_ERR_MISALIGNED;
+  return sai::from_cuda(sai::launch_bounded_wait_selftest(mode, (long long)cycles, status,
+                                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* sai_error_string(int code) {
   switch (code) {
     case SAI_OK: return "ok";

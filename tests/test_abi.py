@@ -236,3 +236,15 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises((ValueError, TypeError)):
         sai.top_k_per_row_decode(t.view(2, 2), torch.zeros(2, dtype=torch.int32), 1, 2, 1,
                                  torch.zeros(2, 1, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("mode,cycles,status,code", [
+    (2, 1000, 0x1000, sai.ERR_INVALID_ARGUMENT),      # no such mode
+    (-1, 1000, 0x1000, sai.ERR_INVALID_ARGUMENT),
+    (0, 0, 0x1000, sai.ERR_INVALID_ARGUMENT),         # cycles out of 1 .. 2^31
+    (1, (1 << 31) + 1, 0x1000, sai.ERR_INVALID_ARGUMENT),
+    (0, 1000, None, sai.ERR_INVALID_ARGUMENT),        # status is required
+    (0, 1000, 0x1002, sai.ERR_MISALIGNED),
+])
+def test_bounded_wait_selftest_argument_validation(lib, mode, cycles, status, code):
+    assert lib.sai_selftest_bounded_wait(mode, cycles, status, None) == code
