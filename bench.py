@@ -70,6 +70,15 @@ def logits_flops(w) -> int:
     return row_tokens(w) * 2 * w.heads * w.head_dim
 
 
+def epilogue_fp32_ops(w) -> int:
+    """FP32 lane operations of the logits epilogue: per row, valid token and
+    head one max (the ReLU) and one fused multiply-add (the weighted sum)."""
+    return row_tokens(w) * w.heads * 2
+
+
+FP32_LANES_PER_SM = 128          # FP32 lanes of a Blackwell SM (4 partitions x 32)
+
+
 def topk_bytes(w) -> int:
     return row_tokens(w) * 4 + w.rows * w.topk * 4
 
@@ -479,6 +488,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     roof["kernel"] = "logits_tc_kernel" + (" (interleaved K)" if il else "") + (" (fused top-k)" if fused else "")
     roof["algorithmic_per_launch"] = lbytes if roof["bound"] == "hbm" else lflops
     roof["peak_source"] = peaks["source"] + (" (fp8 = 2 x measured bf16)" if roof["bound"] == "tensor" else "")
+    # Diagnostic, not a roofline term of the copy/GEMM peaks: the epilogue's
+    # FP32 work at one lane operation per FP32 lane and clock, at the SM clock
+    # sampled during the timed region.
+    clk = clocks.summary()
+    sm_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    t_fp32_ms = epilogue_fp32_ops(w) / (sms * FP32_LANES_PER_SM * sm_mhz * 1e6) * 1e3
+    roof["fp32_epilogue"] = {"ops_per_launch": epilogue_fp32_ops(w), "bound_ms": t_fp32_ms,
+                             "frac_of_kernel_time": t_fp32_ms / lg_ms,
+                             "lanes": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes at {sm_mhz:.0f} MHz"}
     value = tok_all * K / (ms * 1e-3) / 1e9
 
     cpu = None
