@@ -31,6 +31,21 @@ def test_algorithmic_counts_tiny():
     assert bench.logits_bytes(w) == 317 * 132 + 21 * 4 + 2 * 64 * 132 + 2 * 512 * 4 + 8
     assert bench.logits_flops(w) == 317 * 2 * 64 * 128
     assert bench.topk_bytes(w) == 317 * 4 + 2 * 64 * 4
+    assert bench.epilogue_fp32_ops(w) == 317 * 64 * 2
+
+
+def test_algorithmic_counts_mtp_rows_read_k_once_per_request():
+    # next_n = 3, contexts 0, 2, 50, 17 clamped to W = 40: K is read once per
+    # request (0 + 2 + 40 + 17 tokens), while the rows see 0, 1+2, 3 x 40,
+    # 15+16+17 tokens.
+    w = synth.custom(batch=4, next_n=3, heads=64, page_size=8, context_lens=[0, 2, 50, 17],
+                     max_model_len=40, seed=1)
+    assert w.block_table.shape[1] * w.page_size >= 40
+    assert bench.row_tokens(w) == 0 + 3 + 120 + 48
+    assert bench.logits_bytes(w) == (59 * 132 + (0 + 1 + 5 + 3) * 4 + 4 * 3 * 64 * 132
+                                     + 12 * 40 * 4 + 4 * 4)
+    assert bench.logits_flops(w) == 171 * 2 * 64 * 128
+    assert bench.epilogue_fp32_ops(w) == 171 * 64 * 2
 
 
 def _free_port():
