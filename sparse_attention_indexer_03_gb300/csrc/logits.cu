@@ -145,7 +145,12 @@ struct Cfg {
   static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64 +
                                kCtxSmem * 4;
   static constexpr int STAGE_BYTES = IL ? kStageBytesIl : kStageBytes;
-  static constexpr int PER_STAGE = STAGE_BYTES + kScaleSlot + 16 + 16 + (IL ? 8 : 0);
+  // The tile's head weights [next_n, H] fp32 come into the stage with its K
+  // pages when the epilogue's sums are long (N >= 256; page-split caches:
+  // interleaved ones lose a stage to it): read there, not from global memory.
+  static constexpr bool STAGE_W = !IL && N >= 256;
+  static constexpr int W_BYTES = STAGE_W ? NEXT_N * H * 4 : 0;
+  static constexpr int PER_STAGE = STAGE_BYTES + kScaleSlot + 16 + 16 + (IL ? 8 : 0) + W_BYTES;
   static constexpr int FIT = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
   static constexpr int PRODUCERS = ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2;
   static constexpr int STAGES = deepest_sound_ring(FIT, PRODUCERS, C);
@@ -159,16 +164,17 @@ struct Part {        // this CTA's share of the work
 };
 
 struct SmemLayout {
-  uint32_t k, q, sc, meta, ids, bar, misc, ctx, total;
+  uint32_t k, q, sc, meta, wst, ids, bar, misc, ctx, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc, bool il) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int acc, bool il, int w_bytes) {
   SmemLayout L;
   L.k = 0;
   L.q = L.k + stages * (il ? kStageBytesIl : kStageBytes);
   L.sc = L.q + 2 * q_bytes;
   L.meta = L.sc + stages * kScaleSlot;
-  L.ids = L.meta + stages * 16;
+  L.wst = L.meta + stages * 16;                        // per-stage head weights (w_bytes each, may be 0)
+  L.ids = L.wst + stages * w_bytes;
   L.bar = L.ids + kProducers * kLookahead * 32 * 4;
   L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1 + (il ? stages : 0));
   L.ctx = L.misc + 64;
@@ -478,7 +484,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int stages = K::STAGES;
-  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC, IL);
+  const SmemLayout L = smem_layout(stages, K::Q_BYTES, K::ACC, IL, K::W_BYTES);
   const uint32_t s_base = ptx::smem_addr(smem);
   const uint32_t s_k = s_base + L.k, s_q = s_base + L.q;
   float* scales = reinterpret_cast<float*>(smem + L.sc);
@@ -714,7 +720,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
                               (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_expect_tx(stgbar(s), nload * box_bytes);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(stgbar(s), nload * box_bytes + K::W_BYTES);
         __syncwarp();
         if (load) {
           const int y = P > kTile ? (cur.t & 1) * kTile : 0;                     // half of a 256-token page
@@ -722,6 +728,9 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           const uint32_t dst = s_k + s * K::STAGE_BYTES + (P >= kTile ? 0 : pl * box_bytes);
           ptx::bulk_load(dst, src, box_bytes, stgbar(s), pol_k);
         }
+        if (K::STAGE_W && lane == 31)
+          ptx::bulk_load(s_base + L.wst + s * K::W_BYTES, p.weights + (int64_t)cur.b * NEXT_N * H, K::W_BYTES,
+                         stgbar(s), pol_q);
         if (hold) {                                    // rewrite the previous tile while this one lands
           const int prev_s = held_s;
           const uint32_t prev_ph = held_ph;
@@ -745,8 +754,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
                               (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes + K::W_BYTES);
         __syncwarp();
+        if (K::STAGE_W && lane == 31)
+          ptx::bulk_load(s_base + L.wst + s * K::W_BYTES, p.weights + (int64_t)cur.b * NEXT_N * H, K::W_BYTES,
+                         full(s), pol_q);
         if (load) {
           const int y = P > kTile ? (cur.t & 1) * kTile : 0;                       // half of a 256-token page
           const uint32_t dst = s_k + s * kStageBytes + (P >= kTile ? 0 : pl * P * kHeadDim);
@@ -845,18 +857,22 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       if (!ptx::mbar_wait_warp(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
       const int4 m = meta[s];
       const float sc = scales[s * kTile + token];
+      // Weights of the job's rows: float4 f of row c * ROWS + jr is ldw(jr * H / 4 + f).
       const float4* w0 = reinterpret_cast<const float4*>(p.weights + ((int64_t)m.x * NEXT_N + c * K::ROWS) * H);
+      const uint32_t ws0 = s_base + L.wst + s * K::W_BYTES + c * K::ROWS * H * 4;
+      auto ldw = [&](int f) { return K::STAGE_W ? ptx::lds128(ws0 + 16u * f) : __ldg(w0 + f); };
       float4 wn[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) wn[x] = __ldg(w0 + x);
+      for (int x = 0; x < 8; ++x) wn[x] = ldw(x);
       if (!ptx::mbar_wait_warp(tfull(acc), (uint32_t)(a / K::ACC) & 1u, abort_flag, kWaitBudget)) { if (lane == 0) fail(); break; }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(kempty(s));
+      // The stage is released here unless its staged weights are still to be
+      // read by the sums below.
+      if (!K::STAGE_W && lane == 0) ptx::mbar_arrive(kempty(s));
       ptx::tc_fence_after();
       float out[K::ROWS];
 #pragma unroll
       for (int jr = 0; jr < K::ROWS; ++jr) {
-        const float4* wrow = w0 + jr * (H / 4);
         // Eight independent partial sums, held as four pairs updated by
         // paired fp32 FMAs: one dependent chain of H fused multiply-adds would
         // bound the epilogue by FMA latency.
@@ -869,7 +885,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           ptx::tmem_ld_32(t_lane + (uint32_t)(acc * K::NC + jr * H + h0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           float4 w4[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) w4[x] = (jr == 0 && h0 == 0 && x < 8) ? wn[x] : __ldg(wrow + (h0 >> 2) + x);
+          for (int x = 0; x < 16; ++x) w4[x] = (jr == 0 && h0 == 0 && x < 8) ? wn[x] : ldw(jr * (H / 4) + (h0 >> 2) + x);
           ptx::tmem_ld_wait();
           ptx::tmem_regs_ready(v);
 #pragma unroll
@@ -887,7 +903,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
                   ((part[2].x + part[2].y) + (part[3].x + part[3].y));
       }
       ptx::tc_fence_before();
-      __syncwarp();
+      __syncwarp();                                  // every lane's weight reads are done
+      if (K::STAGE_W && lane == 0) ptx::mbar_arrive(kempty(s));
       if (lane == 0) ptx::mbar_arrive(tempty(acc));
       const int64_t col = (int64_t)m.y * kTile + token;
       if (col < p.width) {
@@ -1075,7 +1092,7 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
     }
   }
   if (IL) tkv = tq;                                      // never read
-  const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC, IL);
+  const SmemLayout L = smem_layout(K::STAGES, K::Q_BYTES, K::ACC, IL, K::W_BYTES);
   const size_t smem = (size_t)L.total + 1024;
   if (smem > (size_t)kMaxSmem) return cudaErrorInvalidConfiguration;
   static int smem_set[64] = {0};

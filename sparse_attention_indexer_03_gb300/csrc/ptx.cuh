@@ -114,6 +114,13 @@ __device__ __forceinline__ void launch_dependents() {
 // is visible; a no-op when the launch carried no programmatic dependency.
 __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// 16-byte shared-memory load at a 32-bit shared address.
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its thread-block cluster.
 __device__ __forceinline__ uint32_t cluster_rank() {
