@@ -2,19 +2,25 @@
 """Benchmark of the indexer decode step: FP8 paged MQA logits, then per-row top-k.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|tiny|mtp|wide|kv2g|sweep:P,next_n,H,B,ctx]
+                    [--workload wide|decode|tiny|mtp|kv2g|wide_b<B>|sweep:P,next_n,H,B,ctx]
+                    [--sweep subset|all]
 
 One step = one logits launch plus one top-k launch over one batch of synthetic
-inputs (the decode workload by default: B=64, next_n=1, H=64, D=128, P=64,
-ctx U[1024, 8192], W=8192, k=2048).  Metric: row-tokens per second,
-sum_r ctx_r / time, in Gtok/s, whole job over all ranks.
+inputs (by default the wide workload, the largest configuration on one GPU:
+B=256, next_n=4 -> 1024 rows, H=64, D=128, P=16, ctx U[4096, 16384],
+W = stride = 2^20, k=2048).  Metric: row-tokens per second, sum_r ctx_r /
+time, in Gtok/s, whole job over all ranks.
 
 Timing: inputs are resident in HBM; several input sets rotate so that the
-bytes one cycle touches exceed the 129 MB L2; the K steps run as replays of a
-CUDA graph of S steps, bracketed by a barrier and a device synchronise on
-both sides, timed with CUDA events; the slowest rank's time counts.  A
-second graph of the same steps with timing events around every kernel is
-replayed right after the timed region and gives the per-launch durations.
+bytes one cycle touches exceed the 129 MB L2; each measurement times exactly
+K steps, run as replays of a CUDA graph of S steps, bracketed by a barrier
+and a device synchronise on both sides, with CUDA events; the measurement is
+repeated until about half a second has been timed, and the median
+measurement (the slowest rank's) counts.  A second graph of the same steps
+with timing events around every kernel is replayed after the timed region
+and gives the per-launch durations.
+
+`--sweep` runs the throughput sweep instead (one JSON line per point).
 
 Multi-GPU: one process per GPU (torchrun), each running its own batch of
 requests; no data-path collective (requests are independent), so scaling is
@@ -41,6 +47,7 @@ import numpy as np  # noqa: E402
 METRIC = "indexer Gtokens/s (rows x context tokens) and % of FP8/HBM roofline, 1 GB300"
 UNIT = "Gtok/s"
 L2_BYTES = 129 * 2**20
+MEASURE_SECONDS = 0.5          # timed per bench line, over repeated K-step measurements
 
 
 # ------------------------------------------------------------------ helpers
@@ -99,6 +106,8 @@ def make_workload(name: str, layout: str = "split"):
     if name.startswith("sweep:"):
         p, n, h, b, c = (int(x) for x in name.split(":", 1)[1].split(","))
         return synth.sweep_point(p, n, h, b, c, layout=layout)
+    if name.startswith("wide_b"):
+        return synth.wide(layout, batch=int(name[len("wide_b"):]))
     return synth.NAMED[name](layout)
 
 
@@ -342,24 +351,43 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if probe is not None:
             probe.replay()
     torch.cuda.synchronize()
-
-    if world > 1:
-        dist.barrier()
+    # Rough length of one measurement, to choose how many to take.
+    c0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        graph.replay()
     torch.cuda.synchronize()
+    est = max(1e-6, (time.perf_counter() - c0) * reps)
+    M = max(3, min(2000, math.ceil(MEASURE_SECONDS / est)))
+    if world > 1:                      # every rank takes the same number of measurements
+        m_t = torch.tensor([M], dtype=torch.int64, device=dev)
+        dist.all_reduce(m_t, op=dist.ReduceOp.MAX)
+        M = int(m_t.item())
+
+    # Each measurement times exactly K steps (reps replays of the S-step
+    # graph), bracketed by a barrier and a synchronise on both sides.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    meas = []
     with ClockSampler(local_rank) as clocks:
-        with torch.cuda.stream(stream):          # replay() launches on the current stream
-            t_start.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            t_end.record(stream)
+        for _ in range(M):
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):          # replay() launches on the current stream
+                t_start.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                t_end.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+            meas.append(t_start.elapsed_time(t_end))
+        with torch.cuda.stream(stream):
             if probe is not None:
                 probe.replay()
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    ms = t_start.elapsed_time(t_end)
+    ms = float(np.median(meas))
+    ms_mean = float(np.mean(meas))
     if ev:
         logits_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(S)]
         topk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(S)]
@@ -449,18 +477,26 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e2e_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(e2e_graph, stream=stream):
         e2e_steps()
-    reps_e = max(1, min(args.steps, 200) // E_STEPS)
-    Ke = reps_e * E_STEPS
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e2e_graph.replay()
-        e0.record(stream)
-        for _ in range(reps_e):
-            e2e_graph.replay()
-        e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    c0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e2e_graph.replay()
+    torch.cuda.synchronize()
+    Me = max(3, min(500, math.ceil(0.5 * MEASURE_SECONDS / max(1e-6, time.perf_counter() - c0))))
+    Ke = E_STEPS
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e_meas = []
+    for _ in range(Me):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            e2e_graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e_meas.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.median(e_meas))
     e2e_ms, _ = aggregate(e2e_ms, tok, world, dev)
     assert int(status.item()) == 0, f"status {int(status.item()):#x}"
 
@@ -512,8 +548,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "data": "synthetic",
             "config": {"workload": describe(w), "row_tokens_per_step": tok,
                        "l2": f"{R} rotating input sets, {R * touched / 2**20:.0f} MB touched per cycle > 129 MB L2",
-                       "timing": f"{K // S} replays of a CUDA graph of {S} steps; kernel durations from "
-                                 f"a replay of the same steps with timing events around each kernel",
+                       "timing": f"median of {M} measurements, each of exactly {K} steps ({K // S} replays of a "
+                                 f"CUDA graph of {S} steps, barrier and synchronise on both sides); kernel "
+                                 f"durations from a replay of the same steps with timing events around each kernel",
+                       "ms_per_step_mean": ms_mean / K,
+                       "ms_per_step_min_max": [min(meas) / K, max(meas) / K],
                        "path": ("one fused launch (logits, then top-k by the CTA completing each request)"
                                 if fused else "two launches (logits, top-k)"),
                        "logits_ms": lg_ms, "topk_ms": None if fused else tk_ms,
@@ -527,7 +566,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "how": "per step: one pinned H2D copy of the packed inputs, the step, one D2H copy "
                            "of the indices; two buffer sets alternate so copies overlap kernels; "
-                           "graph of 32 steps replayed"},
+                           f"median of {Me} replays of a graph of {E_STEPS} steps"},
             "gpu_launches": (1 if fused else 2) * K,
             "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
@@ -769,10 +808,10 @@ def run_gather(args, rank: int, world: int, local_rank: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="wide")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["indexer", "kcache", "gather"], default="indexer",
                     help="the indexer decode path (logits, top-k), the K-cache write before it, "

@@ -22,8 +22,12 @@
  *   - Pointers marked "device" must be device memory (or managed memory) of
  *     the current device.  Nothing is read from or written to host memory.
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
- *     never synchronise.  They allocate nothing and keep no state across calls
- *     apart from a per-process cache of the device's SM count.
+ *     never synchronise.  They allocate nothing.  State kept across calls,
+ *     per process: each device's SM count; up to 32 encoded TMA tensor maps,
+ *     keyed by device, buffer address, extent and box (a hit is always valid
+ *     for the buffer it names); per kernel and device, a flag that its
+ *     shared-memory size attribute has been raised; and the static request
+ *     counters of sai_paged_mqa_logits_topk_static (a device array).
  *   - The caller owns every buffer.  The library keeps no pointer after the
  *     call returns (kernels still in flight use them until they finish).
  *   - Return value: SAI_OK (0), or a negative SAI_ERR_* code.  On any error
@@ -215,10 +219,12 @@ SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_ca
  * Arguments and results are those of sai_paged_mqa_logits_topk minus the
  * workspace.  batch > 16384 returns SAI_ERR_WORKSPACE before any CUDA call.
  *
- *   - Set-up: the first call with a given device current looks up the
- *     array's device address on that device (cudaGetSymbolAddress) and keeps
- *     it; a failure there returns SAI_ERR_CUDA.  Make that first call, on
- *     every device used, before any stream capture begins.
+ *   - Set-up: every call looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress; no pointer is kept, so a device
+ *     reset between calls leaves nothing stale); a failure there returns
+ *     SAI_ERR_CUDA.  The first lookup on a device loads the library's module
+ *     there: make the first call, on every device used, before any stream
+ *     capture begins.
  *   - Zero state: the counters are zero when the library is loaded, and every
  *     call that completes leaves them zero.  After a call that raised
  *     SAI_STATUS_TIMEOUT they may hold partial counts, and later calls of

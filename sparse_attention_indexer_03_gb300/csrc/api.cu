@@ -3,7 +3,6 @@
 // nor any output.
 #include <climits>
 #include <cstdint>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -97,22 +96,12 @@ int check_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_page
 constexpr int kStaticMaxBatch = 16384;
 static __device__ __align__(256) int32_t g_static_counters[kStaticMaxBatch];
 
-std::mutex g_static_mu;
-int32_t* g_static_ptr[64] = {};
-
-// Device address of this device's counters, looked up once per device (on
-// the first call made with that device current).
+// Device address of the current device's counters, looked up on every call:
+// a cached address would outlive a cudaDeviceReset, which unloads the module.
 int static_counters(int32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SAI_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return SAI_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_counters) != cudaSuccess || p == nullptr) return SAI_ERR_CUDA;
-    g_static_ptr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_counters) != cudaSuccess || p == nullptr) return SAI_ERR_CUDA;
+  *out = static_cast<int32_t*>(p);
   return SAI_OK;
 }
 

@@ -234,18 +234,21 @@ def mtp(layout: str = LAYOUT_SPLIT) -> Workload:
 WIDE_FIRST_PAGE = 233_017   # first block of 16 above the int32 row limit of 576-byte rows
 
 
-def wide(layout: str = LAYOUT_SPLIT) -> Workload:
+def wide(layout: str = LAYOUT_SPLIT, batch: int = 256) -> Workload:
     """B=256, next_n=4, H=64, P=16, ctx U[4096, 16384], W = stride = 2^20, k=2048.
 
     Pool of 4,000,000 tokens (250,000 pages of 16).  Every request's table row
     is its own random permutation of the pool's top pages [233017, 250000),
     cut to 1024 entries, so rows >= 512 of the logits lie past 2^31 bytes.
+    `batch` < 256 gives the same per-request shape with fewer requests (named
+    wide_b<batch>; a case small enough for a profiler capture).
     """
     rng = np.random.Generator(np.random.PCG64(SEEDS["wide"]))
-    ctx = rng.integers(4096, 16384, size=256, endpoint=True)
+    ctx = rng.integers(4096, 16384, size=batch, endpoint=True)
     top = np.arange(WIDE_FIRST_PAGE, 250_000)
-    table = np.stack([rng.permutation(top)[:1024] for _ in range(256)])
-    return make_workload("wide", batch=256, next_n=4, heads=64, page_size=16,
+    table = np.stack([rng.permutation(top)[:1024] for _ in range(batch)])
+    return make_workload("wide" if batch == 256 else f"wide_b{batch}", batch=batch, next_n=4, heads=64,
+                         page_size=16,
                          max_model_len=1 << 20, logits_stride=1 << 20, topk=2048,
                          context_lens=ctx, block_table=table, num_pages=250_000,
                          rng=rng, seed=SEEDS["wide"], layout=layout)
@@ -354,3 +357,64 @@ def gather_batch(batch: int = 64, next_n: int = 1, k: int = 2048, page_size: int
         m = min(k, n)
         idx[r, :m] = np.sort(rng.choice(n, m, replace=False))
     return idx, table, ctx
+
+
+# ---------------------------------------------------------------- sweep on the device
+@dataclasses.dataclass
+class DeviceWorkload:
+    """A sweep point drawn directly on the device (pools of several GB are
+    too slow to draw on the host).  Same value distributions as the host
+    workloads, from torch's device generator: q and K values N(0, 1) cast to
+    e4m3fn, scales U(0.5, 2), weights N(0, 1) / sqrt(H).  Uniform contexts,
+    W = ctx, row stride ceil(ctx / 4) * 4, pool = exactly the pages the batch
+    needs, randomly permuted into the block table.  For timing only: the
+    parity tests use the host workloads, which the oracle can read."""
+
+    name: str
+    batch: int
+    next_n: int
+    heads: int
+    page_size: int
+    max_model_len: int
+    logits_stride: int
+    topk: int
+    context_lens: np.ndarray    # host copy, int32 [B]
+    block_table: object         # device int32 [B, npg]
+    num_pages: int
+    seed: int
+    dev: dict                   # q, kv, weights, context_lens, block_table on the device
+    head_dim: int = HEAD_DIM
+    layout: str = LAYOUT_SPLIT
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.next_n
+
+
+def sweep_point_device(page_size: int, next_n: int, heads: int, batch: int, ctx: int, device,
+                       seed: int = 0, chunk_pages: int = 1 << 16) -> DeviceWorkload:
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    npg = -(-ctx // page_size)
+    num_pages = batch * npg
+    P = page_size
+    kv = torch.empty(num_pages * P * (HEAD_DIM + SCALE_BYTES), dtype=torch.uint8, device=device)
+    pages = kv.view(num_pages, P * (HEAD_DIM + SCALE_BYTES))
+    for p0 in range(0, num_pages, chunk_pages):
+        p1 = min(num_pages, p0 + chunk_pages)
+        vals = torch.randn((p1 - p0, P * HEAD_DIM), generator=g, device=device)
+        pages[p0:p1, :P * HEAD_DIM] = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+        sc = torch.rand((p1 - p0, P), generator=g, device=device) * 1.5 + 0.5
+        pages[p0:p1, P * HEAD_DIM:] = sc.contiguous().view(torch.uint8)
+        del vals, sc
+    q = torch.randn((batch, next_n, heads, HEAD_DIM), generator=g, device=device)
+    q = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    w = torch.randn((batch * next_n, heads), generator=g, device=device) / math.sqrt(heads)
+    table = torch.randperm(num_pages, generator=g, device=device).to(torch.int32).view(batch, npg)
+    ctx_h = np.full(batch, ctx, np.int32)
+    dev = dict(q=q, kv=kv, weights=w.contiguous(), context_lens=torch.from_numpy(ctx_h).to(device),
+               block_table=table.contiguous())
+    return DeviceWorkload(f"sweep_P{page_size}_n{next_n}_H{heads}_B{batch}_ctx{ctx}", batch, next_n, heads,
+                          page_size, ctx, -(-ctx // 4) * 4, 2048, ctx_h, table, num_pages, int(seed), dev)

@@ -75,7 +75,7 @@ def test_mtp():
     _check(synth.mtp(), oracle=False)
 
 
-@pytest.mark.parametrize("next_n,heads", [(1, 64), (2, 128), (3, 64), (4, 128)])
+@pytest.mark.parametrize("next_n,heads", [(1, 64), (2, 128), (3, 64), (3, 128), (4, 64), (4, 128)])
 @pytest.mark.parametrize("page_size", [8, 64, 256])
 def test_shapes(page_size, next_n, heads):
     w = synth.custom(batch=7, next_n=next_n, heads=heads, page_size=page_size,

@@ -53,7 +53,7 @@ def test_mtp():
 
 
 @pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128, 256])
-@pytest.mark.parametrize("next_n,heads", [(1, 64), (2, 128), (3, 64), (4, 128)])
+@pytest.mark.parametrize("next_n,heads", [(1, 64), (2, 128), (3, 64), (3, 128), (4, 64), (4, 128)])
 def test_page_sizes_and_mtp_rows(page_size, next_n, heads):
     # Ragged everything: contexts not multiples of the page or of 128, an empty
     # request, one shorter than next_n, W not a multiple of 128, stride > W.

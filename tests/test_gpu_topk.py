@@ -141,3 +141,131 @@ def test_rows_split_over_a_cluster_match_one_cta_per_row(W):
         reps = -(-rows // 5)
         again = _run_on_values(np.tile(vals, (reps, 1)), np.tile(ctx, reps), 1, k, W)
         assert (again == np.tile(got, (reps, 1))).all(), rows
+
+
+# ---- the large configurations: rows past byte 2^31, sweep points, KV past 2^31
+
+def assert_topk_exact_on_device(view: torch.Tensor, idx: torch.Tensor, n_r: torch.Tensor, k: int,
+                                what: str, chunk: int = 64):
+    """The top-k property on the GPU's own fp32 logits, for every row, checked
+    on the device (any size): entries [min(k, n_r), k) are -1; the others are
+    distinct columns in [0, n_r); and no column of the row holds a value
+    greater than the smallest selected one unless it is selected too (fewer
+    than min(k, n_r) columns lie strictly above it).  Columns past n_r are
+    -inf, so they never count."""
+    rows = idx.shape[0]
+    m = torch.clamp(n_r, max=k)
+    col = torch.arange(k, device=idx.device)[None, :]
+    live = col < m[:, None]
+    assert bool((idx[~live] == -1).all()), f"{what}: padding not -1"
+    assert bool(((idx >= 0) & (idx < n_r[:, None]))[live].all()), f"{what}: index outside [0, n_r)"
+    srt, _ = torch.sort(torch.where(live, idx, torch.full_like(idx, -1)), dim=1)
+    dup = (srt[:, 1:] == srt[:, :-1]) & (srt[:, 1:] >= 0)
+    assert not bool(dup.any()), f"{what}: duplicate indices"
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        v = view[r0:r1]
+        sel = torch.gather(v, 1, idx[r0:r1].clamp(min=0).long())
+        sel = torch.where(live[r0:r1], sel, torch.full_like(sel, float("inf")))
+        thr = sel.min(dim=1).values
+        above = (v > thr[:, None]).sum(dim=1)
+        full = m[r0:r1] > 0
+        assert bool((above[full] < m[r0:r1][full]).all()), f"{what}: rows {r0}..{r1} miss a larger value"
+
+
+WIDE_ROWS = [0, 1, 510, 511, 512, 513, 767, 1022, 1023]
+
+
+@pytest.mark.slow
+def test_wide_rows_past_2g():
+    """The wide workload (logits [1024, 1<<20] fp32, 4 GiB; rows >= 512 start
+    past byte 2^31 of the buffer, the rows an int32 byte offset loses: aiter
+    PR 4244, "Root cause").  Logits, then top-k, on a sentinel-filled buffer:
+    every row's top-k property on the device; sampled rows (always 510-513,
+    767, 1022, 1023) against the fp64 oracle with the tie tolerance; then
+    the oracle's own fp32 values written into those rows of the same 4 GiB
+    buffer, so they still lie past 2^31 bytes, and the sets exactly equal to
+    the oracle's top-k of those values."""
+    w = synth.wide()
+    logits = torch.full((w.rows, w.logits_stride), 12345.0, dtype=torch.float32, device="cuda")
+    _, view, dev = run_logits(w, logits=logits)
+    idx = run_topk(view, dev, w)
+    torch.cuda.synchronize()
+    n_r = row_ctx(w, cap_table=False)
+    n_dev = torch.from_numpy(n_r).cuda()
+    assert_topk_exact_on_device(view, idx, n_dev, w.topk, "wide")
+    rng = np.random.default_rng(1)
+    sample = sorted(set(WIDE_ROWS + rng.integers(0, w.rows, 8).tolist()))
+    ref = oracle_logits(w, rows=sample, W=int(n_r[sample].max()) + 1)
+    got = idx[sample].cpu().numpy()
+    assert_topk_valid(got, ref, n_r[sample], w.topk, "wide top-k")
+    # The oracle's fp32 values in the same rows of the 4 GiB buffer.
+    ref32 = ref.astype(np.float32)
+    for i, r in enumerate(sample):
+        view[r, :ref32.shape[1]] = torch.from_numpy(ref32[i]).cuda()
+    idx2 = run_topk(view, dev, w)
+    torch.cuda.synchronize()
+    assert_topk_exact(idx2[sample].cpu().numpy(), ref32, n_r[sample], w.topk)
+
+
+@pytest.mark.slow
+def test_wide_fused_rows_past_2g():
+    """The fused logits + top-k launch on the wide workload: logits bit-equal
+    to the logits launch's, indices entry for entry equal to the top-k
+    launch's on them, the top-k property on every row, sampled rows (rows
+    past byte 2^31 always among them) against the oracle."""
+    w = synth.wide()
+    dev = w.to_device()
+    logits = torch.full((w.rows, w.logits_stride), 4321.0, dtype=torch.float32, device="cuda")
+    idx = torch.full((w.rows, w.topk), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(w.batch, dtype=torch.int32, device="cuda")
+    sai.paged_mqa_logits_topk(dev["q"], dev["kv"], w.page_size, dev["weights"], dev["context_lens"],
+                              dev["block_table"], logits, w.max_model_len, w.topk, idx, ws,
+                              num_pages=w.pool.num_pages)
+    torch.cuda.synchronize()
+    assert bool((ws == 0).all())
+    n_r = row_ctx(w, cap_table=False)
+    n_dev = torch.from_numpy(n_r).cuda()
+    assert_topk_exact_on_device(logits, idx, n_dev, w.topk, "wide fused")
+    rng = np.random.default_rng(2)
+    sample = sorted(set(WIDE_ROWS + rng.integers(0, w.rows, 8).tolist()))
+    ref = oracle_logits(w, rows=sample, W=int(n_r[sample].max()) + 1)
+    assert_topk_valid(idx[sample].cpu().numpy(), ref, n_r[sample], w.topk, "wide fused top-k")
+    # Against the two launches, on the same inputs: bit-equal logits, same indices.
+    sep_idx = run_topk(logits, dev, w)
+    torch.cuda.synchronize()
+    assert torch.equal(sep_idx, idx), "fused indices differ from the top-k launch on the fused logits"
+    sep = torch.empty_like(logits)
+    run_logits(w, dev=dev, logits=sep)
+    torch.cuda.synchronize()
+    for r0 in range(0, w.rows, 128):
+        assert torch.equal(sep[r0:r0 + 128], logits[r0:r0 + 128]), f"rows {r0}.. differ"
+
+
+@pytest.mark.slow
+def test_kv_pages_past_2g():
+    """kv-2G: every page lies wholly past byte 2^31 of a 2.24 GB pool."""
+    _both_checks(synth.kv2g())
+
+
+SWEEP_SAMPLE = [(8, 1, 64, 1, 8192), (8, 4, 128, 16, 512), (16, 2, 64, 64, 512),
+                (16, 4, 128, 1, 65536), (64, 1, 128, 16, 8192), (64, 4, 64, 256, 2),
+                (256, 2, 128, 16, 8192), (256, 1, 64, 1, 131072), (256, 4, 128, 64, 512),
+                (16, 1, 64, 16, 131072), (64, 2, 64, 256, 8192)]
+
+
+@pytest.mark.parametrize("pt", SWEEP_SAMPLE, ids=lambda p: "P%d_n%d_H%d_B%d_ctx%d" % p)
+def test_sweep_points(pt):
+    """Sweep points: the top-k property on every row on the device; all rows
+    against the oracle where the oracle is quick, else the first, middle and
+    last rows."""
+    w = synth.sweep_point(*pt)
+    _, view, dev = run_logits(w)
+    idx = run_topk(view, dev, w)
+    torch.cuda.synchronize()
+    n_r = row_ctx(w, cap_table=False)
+    assert_topk_exact_on_device(view[:, :w.max_model_len], idx, torch.from_numpy(n_r).cuda(), w.topk,
+                                "sweep")
+    rows = list(range(w.rows)) if w.rows * w.max_model_len <= 4_000_000 else sorted({0, w.rows // 2, w.rows - 1})
+    ref = oracle_logits(w, rows=rows)
+    assert_topk_valid(idx[rows].cpu().numpy(), ref, n_r[rows], w.topk, "sweep top-k")
