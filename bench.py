@@ -805,6 +805,125 @@ def run_gather(args, rank: int, world: int, local_rank: int):
     return 0
 
 
+# ------------------------------------------------------------------ throughput sweep
+def sweep_subset():
+    """The declared subset: every (P, next_n, H) at B in {64, 256} and ctx in
+    {8192, 65536} (96 of the 600 points)."""
+    import synth
+
+    return [(p, n, h, b, c) for _, p, n, h, b, c in synth.sweep_points() if b in (64, 256) and c in (8192, 65536)]
+
+
+def run_sweep(args, rank: int, world: int, local_rank: int):
+    """One JSON line per sweep point: Gtok/s of the step (logits, then top-k)
+    and the logits kernel against its binding roofline."""
+    import torch
+
+    import sparse_attention_indexer_03_gb300 as sai
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    sai.build()
+    dev = torch.device("cuda", local_rank)
+    if args.sweep == "subset":
+        points = sweep_subset()
+    elif args.sweep == "all":
+        points = [(p, n, h, b, c) for _, p, n, h, b, c in synth.sweep_points()]
+    else:
+        points = [tuple(int(x) for x in pt.split(",")) for pt in args.sweep.split(";")]
+    index = {(p, n, h, b, c): i for i, p, n, h, b, c in synth.sweep_points()}
+    peaks = load_peaks()
+    fp8_peak_tflops = 2.0 * peaks["bf16_tflops"]
+    stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for pt in points:
+        seed = 1000 + index.get(pt, 999)
+        w0 = synth.sweep_point_device(*pt, device=dev, seed=seed)
+        tok = row_tokens(w0)
+        touched = logits_bytes(w0) + topk_bytes(w0)
+        R = max(2, min(16, math.ceil(2.0 * L2_BYTES / max(touched, 1))))
+        sets = [w0.dev] + [synth.sweep_point_device(*pt, device=dev, seed=seed + 7919 * r).dev for r in range(1, R)]
+        for d in sets:
+            d["logits"] = torch.empty((w0.rows, w0.logits_stride), dtype=torch.float32, device=dev)
+            d["indices"] = torch.empty((w0.rows, w0.topk), dtype=torch.int32, device=dev)
+
+        def lcall(d):
+            sai.paged_mqa_logits(d["q"], d["kv"], w0.page_size, d["weights"], d["context_lens"], d["block_table"],
+                                 d["logits"], w0.max_model_len, num_pages=w0.num_pages, status=status, stream=stream)
+
+        def tcall(d):
+            sai.top_k_per_row_decode(d["logits"], d["context_lens"], w0.next_n, w0.max_model_len, w0.topk,
+                                     d["indices"], stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                lcall(sets[i % R])
+                tcall(sets[i % R])
+        torch.cuda.synchronize()
+        S = max(R, min(100, 2 * R * math.ceil(50 / R)))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(S):
+                lcall(sets[i % R])
+                tcall(sets[i % R])
+        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(S)]
+        probe = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(probe, stream=stream):
+            for i in range(S):
+                ev[i][0].record(stream)
+                lcall(sets[i % R])
+                ev[i][1].record(stream)
+                tcall(sets[i % R])
+                ev[i][2].record(stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        c0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        M = max(3, min(200, math.ceil(0.1 / max(1e-6, time.perf_counter() - c0))))
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        meas = []
+        with ClockSampler(local_rank) as clocks:
+            for _ in range(M):
+                torch.cuda.synchronize()
+                with torch.cuda.stream(stream):
+                    t0.record(stream)
+                    graph.replay()
+                    t1.record(stream)
+                torch.cuda.synchronize()
+                meas.append(t0.elapsed_time(t1))
+            with torch.cuda.stream(stream):
+                probe.replay()
+            torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"status {int(status.item()):#x} at {pt}"
+        ms = float(np.median(meas)) / S
+        lg_ms = float(np.median([ev[i][0].elapsed_time(ev[i][1]) for i in range(S)]))
+        tk_ms = float(np.median([ev[i][1].elapsed_time(ev[i][2]) for i in range(S)]))
+        lbytes, lflops = logits_bytes(w0), logits_flops(w0)
+        t_hbm = lbytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = lflops / (fp8_peak_tflops * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        frac = max(t_hbm, t_tc) / (lg_ms * 1e-3)
+        line = {"sweep_point": {"page_size": pt[0], "next_n": pt[1], "heads": pt[2], "batch": pt[3], "ctx": pt[4]},
+                "metric": METRIC, "value": tok / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+                "logits_ms": lg_ms, "topk_ms": tk_ms, "row_tokens_per_step": tok,
+                "roofline": {"bound": bound, "frac": frac,
+                             "achieved": (lbytes / (lg_ms * 1e-3) / 1e9) if bound == "hbm"
+                             else (lflops / (lg_ms * 1e-3) / 1e12),
+                             "peak": peaks["hbm_gbs"] if bound == "hbm" else fp8_peak_tflops,
+                             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                             "algorithmic_per_launch": lbytes if bound == "hbm" else lflops},
+                "timing": f"median of {M} replays of a graph of {S} steps, {R} rotating input sets",
+                "clocks": clocks.summary()}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del sets, graph, probe, w0
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -819,6 +938,9 @@ def main():
     ap.add_argument("--layout", choices=["split", "interleaved"], default="split",
                     help="K-cache layout of the indexer workload (interleaved: pages staged as stored, "
                          "rewritten for the MMA)")
+    ap.add_argument("--sweep", default=None,
+                    help="run the throughput sweep instead: 'subset' (every P, next_n, H at B in {64, 256}, "
+                         "ctx in {8192, 65536}), 'all' (600 points) or 'P,n,H,B,ctx;...'")
     ap.add_argument("--path", choices=["fused", "separate"], default="separate",
                     help="one fused logits + top-k launch per step, or the two launches")
     args = ap.parse_args()
@@ -845,6 +967,8 @@ def main():
             return run_kcache(args, rank, world, local_rank)
         if args.op == "gather":
             return run_gather(args, rank, world, local_rank)
+        if args.sweep:
+            return run_sweep(args, rank, world, local_rank)
         return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:

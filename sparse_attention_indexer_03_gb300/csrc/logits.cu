@@ -475,6 +475,69 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
   }
 }
 
+// -inf fill of the columns past each request's last tile, in units of
+// (row, 4096 columns) taken from a shared counter, so warps with time to
+// spare (producers waiting for ring space, any warp once its role is done)
+// share it.  Each warp keeps its own position in the walk over the
+// requests: the units it takes only move forward.
+template <int NEXT_N>
+struct Filler {
+  const TcParams* p;
+  int* next;
+  int n_units, lane, b;
+  CtxCache cc;
+  int64_t u_in, ucur, fs, chunks;
+
+  __device__ __forceinline__ void init(const TcParams& pp, const Part& pt, int* counter, const int32_t* staged,
+                                       int ln) {
+    p = &pp;
+    next = counter;
+    n_units = pt.n_units;
+    lane = ln;
+    cc.staged = staged;
+    b = pt.fb0;
+    u_in = pt.fu0;
+    ucur = 0;
+    const int64_t ce = n_units > 0 ? ctx_eff(cc.get(pp, b, lane), pp.cap) : 0;
+    fs = min(pp.width, req_tiles(ce) * kTile);
+    chunks = (pp.width - fs + kFillCols - 1) / kFillCols;
+  }
+
+  // Takes and writes one unit; false when none is left.  Warp-uniform.
+  __device__ bool unit() {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(next, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= n_units) return false;
+    u_in += u - ucur;
+    ucur = u;
+    while (u_in >= NEXT_N * chunks && b < p->batch) {   // move to the request holding unit u
+      u_in -= NEXT_N * chunks;
+      ++b;
+      if (b >= p->batch) break;
+      const int64_t ce = ctx_eff(cc.get(*p, b, lane), p->cap);
+      fs = min(p->width, req_tiles(ce) * kTile);
+      chunks = (p->width - fs + kFillCols - 1) / kFillCols;
+    }
+    if (b >= p->batch) return false;                     // never past the last row
+    const int j = (int)(u_in / chunks);
+    const int64_t c0 = fs + (u_in % chunks) * kFillCols;
+    const int64_t c1 = min(p->width, c0 + kFillCols);
+    float* row = p->logits + ((int64_t)b * NEXT_N + j) * p->stride;    // 64-bit row base
+    int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(row + c0) & 15)) & 15) >> 2);
+    head = min(head, c1 - c0);
+    if (lane < head) row[c0 + lane] = -INFINITY;
+    const int64_t v0 = c0 + head;
+    const int64_t nv = (c1 - v0) >> 2;
+    float4* vrow = reinterpret_cast<float4*>(row + v0);
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int64_t x = lane; x < nv; x += 32) vrow[x] = ninf;
+    const int64_t tail0 = v0 + nv * 4;
+    if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
+    return true;
+  }
+};
+
 template <int NEXT_N, int H, bool FUSED, bool IL>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
@@ -688,6 +751,20 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     int held_s = -1;                                   // stage of the held tile, -1 if none
     uint32_t held_ph = 0;
     bool held_bad = false;
+    // While the ring is full the warp writes -inf fill units; once none is
+    // left it waits (bounded).  Only where the fill outweighs the tiles: a
+    // unit (16 KB of stores) would otherwise delay the next tile's copies on
+    // a short, latency-bound launch.
+    Filler<NEXT_N> filler;
+    filler.init(p, pt, fill_next, staged, lane);
+    bool fill_left = pt.n_units > pt.n_tiles;
+    auto wait_filling = [&](uint32_t b, uint32_t parity) -> bool {
+      while (fill_left && !__all_sync(0xffffffffu, ptx::mbar_test(b, parity))) {
+        if (*abort_flag) return false;
+        fill_left = filler.unit();
+      }
+      return ptx::mbar_wait_warp(b, parity, abort_flag, kWaitBudget);
+    };
     // Only the first tile's page ids go out before its K copies; the rest of
     // the lookahead follows them, off the first tile's latency chain.
     issue_ids();
@@ -701,7 +778,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const bool is_last = (cur.t == cur.nt - 1) || (i == pt.n_tiles - 1);
       const int qs = q_seq & 1;
       if (!qok) { ok = false; break; }
-      if (!ptx::mbar_wait_warp(kempty(s), ph ^ 1u, abort_flag, kWaitBudget)) { ok = false; if (lane == 0) fail(); break; }
+      if (!wait_filling(kempty(s), ph ^ 1u)) { ok = false; if (lane == 0) fail(); break; }
       if (j == 0) ptx::cp_async_wait<0>();                    // page ids of this tile have landed
       else ptx::cp_async_wait<kLookahead - 1>();
       const int64_t tok0 = (int64_t)cur.t * kTile + (P >= kTile ? 0 : (int64_t)pl * P);
@@ -929,44 +1006,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   // top-k, the other warps stop taking units as soon as the epilogue is done,
   // join the selection, and all warps finish the fill after it.
   auto run_fill = [&](bool yield_to_tail) {
-    CtxCache cc;
-    cc.staged = staged;
-    int b = pt.fb0;
-    int64_t u_in = pt.fu0, ucur = 0;
-    int64_t ce = pt.n_units > 0 ? ctx_eff(cc.get(p, b, lane), p.cap) : 0;
-    int64_t fs = min(p.width, req_tiles(ce) * kTile);
-    int64_t chunks = (p.width - fs + kFillCols - 1) / kFillCols;
+    Filler<NEXT_N> f;
+    f.init(p, pt, fill_next, staged, lane);
     for (;;) {
       if (yield_to_tail && *epi_done == kEpiWarps) break;   // warp-uniform: one shared word
-      int u = 0;
-      if (lane == 0) u = atomicAdd(fill_next, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (u >= pt.n_units) break;
-      u_in += u - ucur;                                // units only move forward for a warp
-      ucur = u;
-      while (u_in >= NEXT_N * chunks && b < p.batch) {   // move to the request holding unit u
-        u_in -= NEXT_N * chunks;
-        ++b;
-        if (b >= p.batch) break;
-        ce = ctx_eff(cc.get(p, b, lane), p.cap);
-        fs = min(p.width, req_tiles(ce) * kTile);
-        chunks = (p.width - fs + kFillCols - 1) / kFillCols;
-      }
-      if (b >= p.batch) break;                          // never past the last row
-      const int j = (int)(u_in / chunks);
-      const int64_t c0 = fs + (u_in % chunks) * kFillCols;
-      const int64_t c1 = min(p.width, c0 + kFillCols);
-      float* row = p.logits + ((int64_t)b * NEXT_N + j) * p.stride;    // 64-bit row base
-      int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(row + c0) & 15)) & 15) >> 2);
-      head = min(head, c1 - c0);
-      if (lane < head) row[c0 + lane] = -INFINITY;
-      const int64_t v0 = c0 + head;
-      const int64_t nv = (c1 - v0) >> 2;
-      float4* vrow = reinterpret_cast<float4*>(row + v0);
-      const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      for (int64_t x = lane; x < nv; x += 32) vrow[x] = ninf;
-      const int64_t tail0 = v0 + nv * 4;
-      if (tail0 + lane < c1) row[tail0 + lane] = -INFINITY;
+      if (!f.unit()) break;
     }
   };
   if constexpr (FUSED) {

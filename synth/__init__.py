@@ -392,7 +392,7 @@ class DeviceWorkload:
 
 
 def sweep_point_device(page_size: int, next_n: int, heads: int, batch: int, ctx: int, device,
-                       seed: int = 0, chunk_pages: int = 1 << 16) -> DeviceWorkload:
+                       seed: int = 0) -> DeviceWorkload:
     import torch
 
     g = torch.Generator(device=device)
@@ -400,6 +400,7 @@ def sweep_point_device(page_size: int, next_n: int, heads: int, batch: int, ctx:
     npg = -(-ctx // page_size)
     num_pages = batch * npg
     P = page_size
+    chunk_pages = max(1, (1 << 26) // (P * HEAD_DIM))      # 64 M values (256 MB of fp32) per draw
     kv = torch.empty(num_pages * P * (HEAD_DIM + SCALE_BYTES), dtype=torch.uint8, device=device)
     pages = kv.view(num_pages, P * (HEAD_DIM + SCALE_BYTES))
     for p0 in range(0, num_pages, chunk_pages):
