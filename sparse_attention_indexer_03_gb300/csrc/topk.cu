@@ -1,13 +1,15 @@
 // Per-row top-k of the indexer logits (`top_k_per_row_decode`, run right after
 // the logits launch in aiter PR 4244, opening paragraph).
 //
-// One CTA of 1024 threads per row runs the exact radix select of select.cuh
+// One CTA per row runs the exact radix select of select.cuh
 // and writes the row's indices in a deterministic order: the columns above
 // the last bin the select examined, ascending, then the columns taken from
-// that bin, ascending (ties at the k-th largest value: the lowest columns).  Rows of a logical width up to 16384 are held in registers
-// (each thread a run of KPT consecutive columns, read from global memory
-// once); wider rows up to 40960 long are copied into shared memory once their
-// length is known, and longer ones re-read from global memory (mostly L2) on
+// that bin, ascending (ties at the k-th largest value: the lowest columns).
+// Rows of a logical width up to 16384 are held in registers (each thread a
+// run of KPT consecutive columns, read from global memory once).  Wider rows
+// are copied into shared memory once their length is known (up to 40960
+// columns, or 16384 on two CTAs of 512 threads per SM for logical widths
+// beyond that), and longer ones re-read from global memory (mostly L2) on
 // each pass.
 //
 // The kernel is launched as a programmatic dependent of the previous kernel
@@ -203,44 +205,53 @@ topk_cluster_kernel(TopKArgs a) {
                           ClusterPreceding<CL>{totals, rank});
 }
 
-// ---- wider rows: a row of up to kSmemKeys columns has its keys copied into
+// ---- wider rows: a row of up to KEYS columns has its keys copied into
 // shared memory once its length is known (each lane then a run of about
-// n / 512 columns); a longer row is re-read from L2 on every pass ------------
-constexpr int kSmemKeys = 40960;
-constexpr size_t kSmemKeysBytes = kSelectSmem + 4 * (kSmemKeys + 4);
-
-__global__ void __launch_bounds__(kThreads)
+// n / NT columns); a longer row is re-read from L2 on every pass.  For
+// logical widths up to 40960, one CTA of 1024 threads per SM stages every
+// row.  Wider rows (the wide outputs, whose rows hold far fewer context
+// columns than their width) go to CTAs of 512 threads staging up to 16384
+// keys (112 KB), two per SM: the select's phases are latency-bound, so two
+// rows in flight overlap them.
+template <int NT, int KEYS>
+__global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1)
 topk_smem_kernel(TopKArgs a) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
-  __shared__ SelectShared<kThreads> sh;
+  __shared__ SelectShared<NT> sh;
   ptx::wait_prerequisites();
   ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
   const int64_t r = blockIdx.x;
   const int64_t n = row_len(a, r);
   int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
   if (n <= a.k) {
-    write_short_row(out, n, a.k);
+    for (int i = threadIdx.x; i < a.k; i += NT) out[i] = i < n ? i : -1;
     return;
   }
   uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem);
   const float* row = a.logits + r * a.stride;
-  if (n <= kSmemKeys) {
+  if (n <= KEYS) {
     uint32_t* key_base = reinterpret_cast<uint32_t*>(topk_smem + kSelectSmem);
-    const uint32_t* keys = stage_keys<kThreads>(row, (int)n, key_base, threadIdx.x);
-    topk_row_smem<kThreads>(keys, (int)n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
+    const uint32_t* keys = stage_keys<NT>(row, (int)n, key_base, threadIdx.x);
+    topk_row_smem<NT>(keys, (int)n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
   } else {
-    topk_row_stream<kThreads>(row, n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
+    topk_row_stream<NT>(row, n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
   }
 }
 
+constexpr int kSmemKeysWide = 40960;        // 1024 threads, one CTA per SM
+constexpr int kSmemKeysPair = 16384;        // 512 threads, two CTAs per SM
+
+template <int KEYS>
+constexpr size_t smem_keys_bytes() { return kSelectSmem + 4 * ((size_t)KEYS + 4); }
+
 template <typename Kern>
 cudaError_t launch_pdl(Kern kern, unsigned grid, const TopKArgs& a, cudaStream_t stream, int* smem_set,
-                       size_t smem, size_t smem_max, unsigned cluster = 1) {
+                       size_t smem, size_t smem_max, unsigned cluster = 1, unsigned threads = kThreads) {
   cudaError_t e = ensure_dynamic_smem(kern, smem_max, smem_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -263,7 +274,7 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.batch * a.next_n;
   if (rows == 0) return cudaSuccess;
   const unsigned g = (unsigned)rows;
-  static int set4[64], set8[64], set16[64], set_smem[64], set_c2[64], set_c4[64], set_c8[64];
+  static int set4[64], set8[64], set16[64], set_smem[64], set_pair[64], set_c2[64], set_c4[64], set_c8[64];
   // Rows wider than one CTA's registers go to a cluster (16384 columns per
   // CTA) while the grid stays within four CTAs per SM; more rows fill the
   // GPU one CTA each.  (Clusters of 16 CTAs of 8192 columns were slower on a
@@ -281,8 +292,12 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   } else if (a.width <= 4 * kThreads) e = launch_pdl(topk_reg_kernel<4>, g, a, stream, set4, kSelectSmem, kSelectSmem);
   else if (a.width <= 8 * kThreads) e = launch_pdl(topk_reg_kernel<8>, g, a, stream, set8, kSelectSmem, kSelectSmem);
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
-  else e = launch_pdl(topk_smem_kernel, g, a, stream, set_smem,
-                     kSelectSmem + 4 * (size_t)(std::min<int64_t>(a.width, kSmemKeys) + 4), kSmemKeysBytes);
+  else if (a.width <= kSmemKeysWide)
+    e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, a, stream, set_smem,
+                   kSelectSmem + 4 * (size_t)(a.width + 4), smem_keys_bytes<kSmemKeysWide>());
+  else
+    e = launch_pdl(topk_smem_kernel<512, kSmemKeysPair>, g, a, stream, set_pair, smem_keys_bytes<kSmemKeysPair>(),
+                   smem_keys_bytes<kSmemKeysPair>(), 1, 512);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
