@@ -357,7 +357,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         graph.replay()
     torch.cuda.synchronize()
     est = max(1e-6, (time.perf_counter() - c0) * reps)
-    M = max(3, min(2000, math.ceil(MEASURE_SECONDS / est)))
+    M = max(3, min(2000, math.ceil(args.measure_seconds / est)))
     if world > 1:                      # every rank takes the same number of measurements
         m_t = torch.tensor([M], dtype=torch.int64, device=dev)
         dist.all_reduce(m_t, op=dist.ReduceOp.MAX)
@@ -484,7 +484,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     with torch.cuda.stream(stream):
         e2e_graph.replay()
     torch.cuda.synchronize()
-    Me = max(3, min(500, math.ceil(0.5 * MEASURE_SECONDS / max(1e-6, time.perf_counter() - c0))))
+    Me = max(3, min(500, math.ceil(0.5 * args.measure_seconds / max(1e-6, time.perf_counter() - c0))))
     Ke = E_STEPS
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -932,6 +932,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="wide")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--measure-seconds", type=float, default=MEASURE_SECONDS,
+                    help="time to spend on repeated K-step measurements (the median counts)")
     ap.add_argument("--op", choices=["indexer", "kcache", "gather"], default="indexer",
                     help="the indexer decode path (logits, top-k), the K-cache write before it, "
                          "or the consumer's gather of the selected KV rows after it")
