@@ -283,7 +283,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         d = w.to_device(dev)
         d["logits"] = torch.empty((w.rows, w.logits_stride), dtype=torch.float32, device=dev)
         d["indices"] = torch.empty((w.rows, w.topk), dtype=torch.int32, device=dev)
-        d["ws"] = torch.zeros(max(1, w.batch), dtype=torch.int32, device=dev)
+        d["ws"] = torch.zeros(max(1, sai.logits_topk_workspace_bytes(w.batch) // 4), dtype=torch.int32, device=dev)
         sets.append(d)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -553,7 +553,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  f"durations from a replay of the same steps with timing events around each kernel",
                        "ms_per_step_mean": ms_mean / K,
                        "ms_per_step_min_max": [min(meas) / K, max(meas) / K],
-                       "path": ("one fused launch (logits, then top-k by the CTA completing each request)"
+                       "path": ("one fused launch (logits; rows of completed requests queued and selected by "
+                                "every CTA while its other warps write the -inf fill)"
                                 if fused else "two launches (logits, top-k)"),
                        "logits_ms": lg_ms, "topk_ms": None if fused else tk_ms,
                        "logits_ms_median": float(np.median(logits_ms)),

@@ -166,8 +166,10 @@ SAI_API int sai_top_k_per_row_decode(const float* logits, int64_t logits_stride,
 
 /*
  * sai_paged_mqa_logits_topk_workspace_bytes -- bytes of device workspace that
- * sai_paged_mqa_logits_topk needs for `batch` requests: one int32 counter per
- * request (0 for batch < 0).
+ * sai_paged_mqa_logits_topk needs for `batch` requests: 4 * (5 * batch + 4)
+ * (a tile counter per request, a queue of up to four rows per request, its
+ * head, tail and done count, and a counter of -inf fill units; 0 for
+ * batch <= 0, which launches nothing).
  */
 SAI_API size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch);
 
@@ -192,8 +194,15 @@ SAI_API size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch);
  *
  * How the launch joins the two steps: each CTA, once its logits are stored,
  * adds the number of tiles it computed for a request to that request's
- * counter; the CTA whose addition completes the request selects the
- * request's rows.  No CTA waits for another.
+ * counter; the CTA whose addition completes the request pushes the
+ * request's rows onto a queue of ready rows in the workspace.  Every CTA,
+ * once its own tiles are done, takes rows from the queue and selects them
+ * while its other warps write the -inf fill, whose units all CTAs take from
+ * one counter in the workspace (a CTA that selects less fills more).  A CTA waiting for a queue
+ * entry whose request is still being computed elsewhere waits at most
+ * about one second of SM clock (SAI_STATUS_TIMEOUT, incomplete indices).
+ * The launch needs every one of its CTAs resident at once: it launches one
+ * CTA per SM of the device, so a context restricted to fewer SMs times out.
  */
 SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache,
                               int64_t num_pages, int32_t page_size,
@@ -213,8 +222,9 @@ SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_ca
  * callers that cannot allocate or lend device memory: an engine whose device
  * memory plan is fixed before it runs, a plugin interface that passes only a
  * kernel's inputs and outputs, a C caller with no CUDA allocator at hand.  It
- * allocates nothing either: the per-request counters live in a static device
- * array of 16384 int32 (64 KB) inside libsai.
+ * allocates nothing either: its workspace (request counters and ready-row
+ * queue) is a static device array of 5 * 16384 + 4 int32 (320 KB) inside
+ * libsai.
  *
  * Arguments and results are those of sai_paged_mqa_logits_topk minus the
  * workspace.  batch > 16384 returns SAI_ERR_WORKSPACE before any CUDA call.
@@ -225,12 +235,13 @@ SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_ca
  *     SAI_ERR_CUDA.  The first lookup on a device loads the library's module
  *     there: make the first call, on every device used, before any stream
  *     capture begins.
- *   - Zero state: the counters are zero when the library is loaded, and every
- *     call that completes leaves them zero.  After a call that raised
- *     SAI_STATUS_TIMEOUT they may hold partial counts, and later calls of
- *     this entry point on that device may select from incomplete rows: use
- *     sai_paged_mqa_logits_topk with a zeroed workspace from then on.
- *   - Concurrency: all calls on one device share the counters.  Two calls in
+ *   - Zero state: the array is zero when the library is loaded, and every
+ *     call that completes leaves it zero.  After a call that raised
+ *     SAI_STATUS_TIMEOUT it may hold partial counts and queue entries, and
+ *     later calls of this entry point on that device may select from
+ *     incomplete rows: use sai_paged_mqa_logits_topk with a zeroed workspace
+ *     from then on.
+ *   - Concurrency: all calls on one device share the array.  Two calls in
  *     flight at once (on different streams, or from different threads
  *     without ordering) race on them and give wrong indices; order such calls
  *     on one stream.

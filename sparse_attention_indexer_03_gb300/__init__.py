@@ -205,8 +205,8 @@ def paged_mqa_logits_topk(q, kv_cache, page_size: int, weights, context_lens, bl
 
     Arguments as `paged_mqa_logits` (page-split caches only) plus
     indices    int32 [B * next_n, >= k] (row stride from the tensor)
-    workspace  CUDA tensor of >= logits_topk_workspace_bytes(B) bytes, zero
-               before the first call; every call leaves it zero again.
+    workspace  CUDA tensor of >= logits_topk_workspace_bytes(B) bytes (4 * (5 B + 4)),
+               zero before the first call; every call leaves it zero again.
     """
     import torch
 

@@ -90,11 +90,16 @@ int check_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_page
   return SAI_OK;
 }
 
-// Request counters of sai_paged_mqa_logits_topk_static, for callers that
-// cannot hand the library any memory of their own.  Zero when the module is
-// loaded; every call that completes leaves them zero again.
+// Words of the fused launch's workspace for `batch` requests: a tile counter
+// per request, a queue of up to 4 rows per request (next_n <= 4), its head,
+// tail and done count, and the -inf fill's unit counter.
+constexpr int64_t fused_workspace_words(int64_t batch) { return 5 * batch + 4; }
+
+// The fused launch's workspace for sai_paged_mqa_logits_topk_static, for
+// callers that cannot hand the library any memory of their own.  Zero when
+// the module is loaded; every call that completes leaves it zero again.
 constexpr int kStaticMaxBatch = 16384;
-static __device__ __align__(256) int32_t g_static_counters[kStaticMaxBatch];
+static __device__ __align__(256) int32_t g_static_counters[fused_workspace_words(kStaticMaxBatch)];
 
 // Device address of the current device's counters, looked up on every call:
 // a cached address would outlive a cudaDeviceReset, which unloads the module.
@@ -129,7 +134,7 @@ int sai_paged_mqa_logits(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t 
 }
 
 size_t sai_paged_mqa_logits_topk_workspace_bytes(int32_t batch) {
-  return batch < 0 ? 0 : (size_t)batch * sizeof(int32_t);
+  return batch <= 0 ? 0 : (size_t)sai::fused_workspace_words(batch) * sizeof(int32_t);
 }
 
 int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
@@ -148,8 +153,9 @@ int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_cache, int
   if (k > 65536 || max_model_len > INT32_MAX) return SAI_ERR_UNSUPPORTED;
   if (indices_stride > (INT64_MAX / 8) / ((int64_t)batch * next_n + 1)) return SAI_ERR_INVALID_ARGUMENT;
   if (!aligned(indices, 4) || !aligned(workspace, 4)) return SAI_ERR_MISALIGNED;
-  if (workspace == nullptr || workspace_bytes < (size_t)batch * sizeof(int32_t)) return SAI_ERR_WORKSPACE;
   if (batch == 0) return SAI_OK;
+  if (workspace == nullptr || workspace_bytes < (size_t)fused_workspace_words(batch) * sizeof(int32_t))
+    return SAI_ERR_WORKSPACE;
   a.indices = indices; a.idx_stride = indices_stride; a.k = k;
   a.req_counter = static_cast<int32_t*>(workspace);
   return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -89,7 +89,8 @@ struct TcParams {
   int32_t* indices;
   int64_t idx_stride;
   int k;
-  int32_t* req_counter;   // [batch] tiles counted in so far, zero between launches
+  int32_t* req_counter;   // fused top-k workspace, zero between launches: [batch] tiles counted in
+                          // so far, [4 * batch] ready-row queue, head, tail, done
 };
 
 // Batches up to this many requests have their context lengths copied into
@@ -161,6 +162,8 @@ struct Cfg {
 struct Part {        // this CTA's share of the work
   int b0, t0, n_tiles;
   int fb0, fu0, n_units;
+  int n_sel;         // rows longer than k (the fused top-k's queue length)
+  int u_total;       // fill units of the launch where they outweigh its tiles four times over (else -1)
 };
 
 struct SmemLayout {
@@ -225,6 +228,8 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
   const int64_t G = gridDim.x, cta = blockIdx.x;
   int b0 = 0, t0 = 0, fb0 = 0, fu0 = 0;
   int64_t tb = 0, te = 0, ub = 0, ue = 0;
+  int64_t with_tiles = 0;                            // rows longer than k (per lane, then summed)
+  int64_t u_all = -1;                                // fill units of a fill-heavy launch
   bool clamped = false;
   static_assert(32 * kCtxRegs == kCtxSmem, "every request of a staged batch is read by the register path");
   if (p.batch <= 32 * kCtxRegs) {
@@ -243,9 +248,12 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
       ul[x] = v ? (int32_t)req_units<NEXT_N>(ce, p.width) : 0;
       lt += tl[x];
       lu += ul[x];
+      if (v && p.k > 0)
+        for (int j = 0; j < NEXT_N; ++j) with_tiles += row_context(raw, NEXT_N, j, p.cap) > p.k ? 1 : 0;
     }
     const int64_t it = warp_incl_scan64(lt, lane), iu = warp_incl_scan64(lu, lane);
     const int64_t T = __shfl_sync(0xffffffffu, it, 31), U = __shfl_sync(0xffffffffu, iu, 31);
+    u_all = U > 4 * T ? U : -1;
     tb = split_begin(T, G, cta); te = split_begin(T, G, cta + 1);
     ub = split_begin(U, G, cta); ue = split_begin(U, G, cta + 1);
     int fb = -1, ft = 0, gb = -1, gu = 0;
@@ -268,9 +276,12 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
       const int64_t ce = ctx_eff(raw, p.cap);
       T += req_tiles(ce);
       U += req_units<NEXT_N>(ce, p.width);
+      if (p.k > 0)
+        for (int j = 0; j < NEXT_N; ++j) with_tiles += row_context(raw, NEXT_N, j, p.cap) > p.k ? 1 : 0;
     }
     T = warp_sum64(T);
     U = warp_sum64(U);
+    u_all = U > 4 * T ? U : -1;
     tb = split_begin(T, G, cta); te = split_begin(T, G, cta + 1);
     ub = split_begin(U, G, cta); ue = split_begin(U, G, cta + 1);
     int64_t ct = 0, cu = 0;
@@ -301,9 +312,12 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
     }
   }
   if (blockIdx.x == 0 && __any_sync(0xffffffffu, clamped) && lane == 0) raise_status(p.status, SAI_STATUS_CTX_CLAMPED);
+  with_tiles = warp_sum64(with_tiles);
   if (lane == 0) {
     part->b0 = b0; part->t0 = t0; part->n_tiles = (int)(te - tb);
     part->fb0 = fb0; part->fu0 = fu0; part->n_units = (int)(ue - ub);
+    part->n_sel = (int)with_tiles;
+    part->u_total = u_all < (int64_t(1) << 30) ? (int)u_all : -1;
   }
 }
 
@@ -368,103 +382,178 @@ struct Cursor {
   }
 };
 
-// ---- fused top-k: the CTA that completes a request selects its rows ---------
+// ---- fused top-k: rows go to a ready queue, every CTA selects from it ---------
 // Each CTA adds, per request it touched, the number of that request's tiles it
-// processed to req_counter[b] once its logits are stored and fenced; the CTA
-// whose addition completes the request's tile count resets the counter to 0
-// and runs the top-k of the request's rows, reading them through L2.  No CTA
-// ever waits for another.  Requests without tiles get their -1 rows from CTA
-// (b mod grid).  Runs on all warps of the CTA once its roles and its share of
-// the -inf fill are done (named barrier 1); the drained K-stage ring holds the
-// selection's histograms.
-constexpr int kFusedThreads = kThreadsTc;
-constexpr int kOwnMax = 64;
-
+// processed to the request's counter once its logits are stored and fenced;
+// the CTA whose addition completes the request's tile count resets the
+// counter to 0 and pushes the request's rows onto a queue of ready rows.
+// Every CTA, once its tiles are done, takes rows from the queue (one atomic
+// on its head per row) and selects them, reading the logits through L2; so
+// the selection is spread over the whole grid and starts as soon as a
+// request is complete.  A queue entry not yet written (its request still has
+// tiles in flight on another CTA) is waited for, with a bounded wait; the
+// grid is one CTA per SM, so every CTA is resident.  The last CTA to finish
+// resets the queue's head and tail; the workspace is all zero again.
+// Requests without tiles get their -1 rows from CTA (b mod grid).  Where
+// the -inf fill outweighs the tiles (more than four fill units per tile) the
+// two epilogue warpgroups select (NT = 256) while the other warps keep
+// writing the fill; elsewhere all warps select (NT = 384).  Named barrier 1
+// joins the selecting threads; the drained K-stage ring and Q slots hold the
+// selection's histograms and staged keys.
+template <int NT>
 struct TailBar {
-  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 384;" ::: "memory"); }
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 };
 
-// `ring` is the drained part of shared memory (K stages and Q slots, `ring_bytes`
-// long): the histograms, the group's shared words, the list of requests to
-// select, then the keys of rows that fit (longer rows are re-read from L2).
-template <int NEXT_N>
+__device__ __forceinline__ bool fill_heavy(const Part& pt) { return pt.n_units > 4 * pt.n_tiles; }
+
+template <int NEXT_N, int NT>
 __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int ring_bytes, int etid,
                            const int32_t* staged, const volatile int* abort_flag) {
   auto ctx_of = [&](int b) -> int64_t { return staged ? staged[b] : p.context_lens[b]; };
-  constexpr int NT = kFusedThreads;
-  static_assert(NT == 384, "named barrier 1 counts 384 threads");
-  const TailBar ebar;
+  static_assert(NT == 256 || NT == 384, "the epilogue warpgroups, or every warp of the CTA");
+  const TailBar<NT> ebar;
   uint32_t* hist = reinterpret_cast<uint32_t*>(ring);
   auto* sh = reinterpret_cast<SelectShared<NT>*>(ring + kSelectSmem);
-  int* own = reinterpret_cast<int*>(ring + kSelectSmem + 512);   // [0] count (-1: stop), [1] more, [2..] requests
+  volatile int* word = reinterpret_cast<volatile int*>(ring + kSelectSmem + 512);   // [0] row, [1] done count
+  int* done_list = reinterpret_cast<int*>(ring + kSelectSmem + 520);           // requests completed here
+  constexpr int kDoneMax = (1024 - 520) / 4;
   uint32_t* key_base = reinterpret_cast<uint32_t*>(ring + kSelectSmem + 1024);
   const int key_cap = (ring_bytes - (int)kSelectSmem - 1024) / 4 - 3;
+  int32_t* counter = p.req_counter;
+  int32_t* queue = p.req_counter + p.batch;
+  int32_t* qctl = p.req_counter + 5 * (int64_t)p.batch;     // head, tail, done
   const int k = p.k;
+  const int lane = etid & 31;
+  auto write_short = [&](int64_t row, int64_t n, int tid, int nthreads) {
+    int32_t* out = p.indices + row * p.idx_stride;          // 64-bit row base
+    for (int i = tid; i < k; i += nthreads) out[i] = i < n ? i : -1;
+  };
   __threadfence();                                   // this thread's logits are visible device-wide
   ebar();
-  // The first warp walks this CTA's tiles 32 requests at a time: lane l takes
-  // request b + l, so one round trip of atomics covers 32 requests.
-  int b = pt.b0, left = pt.n_tiles;
-  int64_t t = pt.t0;
-  const int lane = etid & 31;
-  for (;;) {
-    if (etid < 32) {
-      int n_own = 0;
-      const bool stop = *abort_flag != 0;
-      while (!stop && left > 0 && n_own + 32 <= kOwnMax) {
+  // Publish: the first warp walks this CTA's tiles 32 requests at a time
+  // (lane l takes request b + l).  Of each request it completes, the rows
+  // longer than k go onto the queue; the others (indices 0 .. n - 1, then
+  // -1) are written here, by the whole group from a list of the completed
+  // requests (by the warp itself once the list is full).
+  int h_next = -1;                                   // the next queue entry this CTA takes (thread 0)
+  if (etid < 32) {
+    int n_done = 0;
+    if (*abort_flag == 0) {
+      int b = pt.b0, left = pt.n_tiles;
+      int64_t t = pt.t0;
+      while (left > 0) {
         const int bb = b + lane;
-        const int64_t nt = bb < p.batch ? req_tiles(ctx_eff(ctx_of(bb), p.cap)) : 0;
+        const int64_t raw = bb < p.batch ? ctx_of(bb) : 0;
+        const int64_t nt = bb < p.batch ? req_tiles(ctx_eff(raw, p.cap)) : 0;
         const int64_t avail = lane == 0 ? nt - t : nt;
         const int64_t incl = warp_incl_scan64(avail, lane);
         const int64_t m = min(avail, max((int64_t)0, (int64_t)left - (incl - avail)));
-        bool mine = false;
+        bool done = false;
         if (m > 0) {
-          const int old = atomicAdd(&p.req_counter[bb], (int)m);
-          mine = (int64_t)old + m == nt;
-          if (mine) p.req_counter[bb] = 0;             // the last contributor restores zero
+          const int old = atomicAdd(&counter[bb], (int)m);
+          done = (int64_t)old + m == nt;
+          if (done) counter[bb] = 0;                 // the last contributor restores zero
         }
-        const uint32_t ob = __ballot_sync(0xffffffffu, mine);
-        if (mine) own[2 + n_own + __popc(ob & ((1u << lane) - 1u))] = bb;
-        n_own += __popc(ob);
+        int n_long = 0;
+        if (done)
+          for (int j = 0; j < NEXT_N; ++j) n_long += row_context(raw, NEXT_N, j, p.cap) > k ? 1 : 0;
+        const uint32_t db = __ballot_sync(0xffffffffu, done);
+        const int long_incl = __reduce_add_sync(0xffffffffu, n_long);
+        int base = 0;
+        if (lane == 0 && long_incl > 0) base = atomicAdd(&qctl[1], long_incl);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        // Every contributor fenced its logits before its addition, which a
+        // completing lane's addition observed: fence, then publish the rows.
+        if (done) __threadfence();
+        // Each completing lane's queue position: the long rows of the lanes below it.
+        int excl = n_long;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, excl, o);
+          if (lane >= o) excl += y;
+        }
+        excl -= n_long;
+        if (done) {
+          int pos = base + excl;
+          for (int j = 0; j < NEXT_N; ++j)
+            if (row_context(raw, NEXT_N, j, p.cap) > k) atomicExch(&queue[pos++], bb * NEXT_N + j + 1);
+        }
+        // The short rows: through the list, or by this warp once it is full.
+        const int rank = __popc(db & ((1u << lane) - 1u));
+        const bool listed = done && n_done + rank < kDoneMax;
+        if (listed) done_list[n_done + rank] = bb;
+        if (done && !listed)
+          for (int j = 0; j < NEXT_N; ++j) {
+            const int64_t n = row_context(raw, NEXT_N, j, p.cap);
+            if (n <= k) {
+              int32_t* out = p.indices + ((int64_t)bb * NEXT_N + j) * p.idx_stride;
+              for (int i = 0; i < k; ++i) out[i] = i < n ? i : -1;
+            }
+          }
+        n_done = min(kDoneMax, n_done + __popc(db));
         const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total >= left) {
-          left = 0;
-        } else {
-          left -= (int)total;
-          b += 32;
-          t = 0;
+        if (total >= left) break;
+        left -= (int)total;
+        b += 32;
+        t = 0;
+      }
+    }
+    if (lane == 0) word[1] = n_done;
+    if (etid == 0 && *abort_flag == 0 && pt.n_sel > 0) h_next = atomicAdd(&qctl[0], 1);
+  }
+  ebar();
+  {
+    const int n_done = word[1];
+    for (int x = 0; x < n_done; ++x) {
+      const int bb = done_list[x];
+      const int64_t raw = ctx_of(bb);
+      for (int j = 0; j < NEXT_N; ++j) {
+        const int64_t n = row_context(raw, NEXT_N, j, p.cap);
+        if (n <= k) write_short((int64_t)bb * NEXT_N + j, n, etid, NT);
+      }
+    }
+  }
+  // Select: one row at a time from the queue, until past its last long row.
+  // Thread 0 takes the entry after the current one before the group selects
+  // the current row, so the atomic's round trip overlaps the work.
+  for (;;) {
+    if (etid == 0) {
+      int row = -1;
+      const int h = *abort_flag ? pt.n_sel : h_next;
+      if (h >= 0 && h < pt.n_sel) {
+        const long long t0 = clock64();
+        int v;
+        while ((v = atomicAdd(&queue[h], 0)) == 0) {
+          if (*abort_flag || clock64() - t0 > kWaitBudget) {
+            raise_status(p.status, SAI_STATUS_TIMEOUT);
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (v != 0) {
+          queue[h] = 0;
+          row = v - 1;
+          __threadfence();                           // the row's logits, from every CTA that wrote them
+          h_next = atomicAdd(&qctl[0], 1);
         }
       }
-      if (lane == 0) {
-        own[0] = stop ? -1 : n_own;
-        own[1] = (!stop && left > 0) ? 1 : 0;
-      }
-      __threadfence();                               // the other CTAs' logits before the reads below
+      word[0] = row;
     }
     ebar();
-    const int n_own = own[0], more = own[1];
-    if (n_own < 0) return;                           // a wait timed out: leave the rest
-    for (int o = 0; o < n_own; ++o) {
-      const int bb = own[2 + o];
-      const int64_t raw = ctx_of(bb);
-#pragma unroll 1
-      for (int j = 0; j < NEXT_N; ++j) {
-        const int64_t r = (int64_t)bb * NEXT_N + j;
-        const int64_t n = row_context(raw, NEXT_N, j, p.cap);
-        int32_t* out = p.indices + r * p.idx_stride;  // 64-bit row base
-        const float* row = p.logits + r * p.stride;
-        if (n <= k) {
-          for (int i = etid; i < k; i += NT) out[i] = i < n ? i : -1;
-        } else if (n <= key_cap) {
-          const uint32_t* keys = stage_keys<NT>(row, (int)n, key_base, etid);
-          topk_row_smem<NT>(keys, (int)n, k, out, *sh, hist, etid, ebar);
-        } else {
-          topk_row_stream<NT>(row, n, k, out, *sh, hist, etid, ebar);
-        }
-      }
+    const int row = word[0];
+    if (row < 0) break;
+    const int bb = row / NEXT_N, j = row - bb * NEXT_N;
+    const int64_t n = row_context(ctx_of(bb), NEXT_N, j, p.cap);
+    int32_t* out = p.indices + (int64_t)row * p.idx_stride;  // 64-bit row base
+    const float* lrow = p.logits + (int64_t)row * p.stride;
+    if (n <= key_cap) {
+      const uint32_t* keys = stage_keys<NT>(lrow, (int)n, key_base, etid);
+      topk_row_smem<NT>(keys, (int)n, k, out, *sh, hist, etid, ebar);
+    } else {
+      topk_row_stream<NT>(lrow, n, k, out, *sh, hist, etid, ebar);
     }
-    ebar();                                          // own[] read by all before it is rewritten
-    if (!more) break;
+    ebar();                                          // word[0] read by all before it is rewritten
   }
   for (int bb = blockIdx.x; bb < p.batch; bb += gridDim.x) {
     if (req_tiles(ctx_eff(ctx_of(bb), p.cap)) != 0) continue;
@@ -476,27 +565,37 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
 }
 
 // -inf fill of the columns past each request's last tile, in units of
-// (row, 4096 columns) taken from a shared counter, so warps with time to
-// spare (producers waiting for ring space, any warp once its role is done)
-// share it.  Each warp keeps its own position in the walk over the
-// requests: the units it takes only move forward.
+// (row, 4096 columns) taken from a counter, so warps with time to spare
+// (producers waiting for ring space, any warp once its role is done) share
+// it.  Each warp keeps its own position in the walk over the requests: the
+// units it takes only move forward.  By default each CTA fills its own
+// share of the units from a shared-memory counter.  The fused launch, whose
+// CTAs spend unequal times selecting rows, shares every unit of the launch
+// through one counter in global memory instead (`whole` set), so the CTAs
+// that select less fill more; a warp that fills until its role is done
+// takes kClaim units at a time there (`batch`), a warp that fills only
+// while it waits takes one, so that it never drops units it has claimed.
+constexpr int kClaim = 4;
+
 template <int NEXT_N>
 struct Filler {
   const TcParams* p;
   int* next;
-  int n_units, lane, b;
+  int n_units, lane, b, step, claim, claim_end;
   CtxCache cc;
   int64_t u_in, ucur, fs, chunks;
 
   __device__ __forceinline__ void init(const TcParams& pp, const Part& pt, int* counter, const int32_t* staged,
-                                       int ln) {
+                                       int ln, bool whole = false, bool batch = false) {
     p = &pp;
     next = counter;
-    n_units = pt.n_units;
+    n_units = whole ? pt.u_total : pt.n_units;
+    step = whole && batch ? kClaim : 1;
+    claim = claim_end = 0;
     lane = ln;
     cc.staged = staged;
-    b = pt.fb0;
-    u_in = pt.fu0;
+    b = whole ? 0 : pt.fb0;
+    u_in = whole ? 0 : pt.fu0;
     ucur = 0;
     const int64_t ce = n_units > 0 ? ctx_eff(cc.get(pp, b, lane), pp.cap) : 0;
     fs = min(pp.width, req_tiles(ce) * kTile);
@@ -505,10 +604,15 @@ struct Filler {
 
   // Takes and writes one unit; false when none is left.  Warp-uniform.
   __device__ bool unit() {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(next, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u >= n_units) return false;
+    if (claim >= claim_end) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(next, step);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= n_units) return false;
+      claim = u;
+      claim_end = min(n_units, u + step);
+    }
+    const int u = claim++;
     u_in += u - ucur;
     ucur = u;
     while (u_in >= NEXT_N * chunks && b < p->batch) {   // move to the request holding unit u
@@ -565,7 +669,6 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   int* fill_next = reinterpret_cast<int*>(smem + L.misc + 8);      // next -inf fill unit to take
-  volatile int* epi_done = reinterpret_cast<volatile int*>(smem + L.misc + 12);   // epilogue warps finished
   Part* part = reinterpret_cast<Part*>(smem + L.misc + 16);
   int32_t* ctx_s = reinterpret_cast<int32_t*>(smem + L.ctx);
   const int32_t* staged = p.batch <= kCtxSmem ? ctx_s : nullptr;   // written by the partition
@@ -606,7 +709,6 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         for (int s = 0; s < stages; ++s) ptx::mbar_init(stgbar(s), 1);
       *abort_flag = 0;
       *fill_next = 0;
-      *epi_done = 0;
       ptx::fence_barrier_init();
     }
     __syncwarp();
@@ -618,6 +720,12 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const Part pt = *part;
+  // A fused launch whose fill outweighs its tiles four times over fills from
+  // one counter for the whole grid (the word after the ready queue's head,
+  // tail and done count); the choice is the same for every CTA.  Elsewhere
+  // the producers' fill while they wait would pay a global atomic per unit.
+  const bool whole_fill = FUSED && pt.u_total >= 0;
+  int* fill_ctr = whole_fill ? p.req_counter + 5 * (int64_t)p.batch + 3 : fill_next;
   // The next kernel in the stream (top-k) may be scheduled now; it still
   // waits for this grid to complete before it reads the logits.
   ptx::launch_dependents();
@@ -756,7 +864,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     // unit (16 KB of stores) would otherwise delay the next tile's copies on
     // a short, latency-bound launch.
     Filler<NEXT_N> filler;
-    filler.init(p, pt, fill_next, staged, lane);
+    filler.init(p, pt, fill_ctr, staged, lane, whole_fill);
     bool fill_left = pt.n_units > pt.n_tiles;
     auto wait_filling = [&](uint32_t b, uint32_t parity) -> bool {
       while (fill_left && !__all_sync(0xffffffffu, ptx::mbar_test(b, parity))) {
@@ -994,31 +1102,29 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         }
       }
     }
-    if constexpr (FUSED) {
-      __syncwarp();
-      if (lane == 0) atomicAdd(const_cast<int*>(epi_done), 1);
-    }
   }
 
   // ---- -inf fill past each request's last tile --------------------------------
-  // Every warp takes units from a shared counter once its role is done, so the
-  // warps that finish first (the producers) do most of it.  With the fused
-  // top-k, the other warps stop taking units as soon as the epilogue is done,
-  // join the selection, and all warps finish the fill after it.
-  auto run_fill = [&](bool yield_to_tail) {
+  // Every warp takes units from a shared counter once its role is done (the
+  // producers also while they wait for ring space).  With the fused top-k the
+  // epilogue warps select rows first and then join the fill.
+  auto run_fill = [&]() {
     Filler<NEXT_N> f;
-    f.init(p, pt, fill_next, staged, lane);
-    for (;;) {
-      if (yield_to_tail && *epi_done == kEpiWarps) break;   // warp-uniform: one shared word
-      if (!f.unit()) break;
+    f.init(p, pt, fill_ctr, staged, lane, whole_fill, true);
+    while (f.unit()) {
     }
   };
   if constexpr (FUSED) {
-    if (warp < kFirstEpiWarp) run_fill(true);
-    fused_topk<NEXT_N>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x, staged, abort_flag);
-    run_fill(false);
+    if (fill_heavy(pt)) {      // the epilogue warpgroups select rows while the other warps fill
+      if (warp >= kFirstEpiWarp)
+        fused_topk<NEXT_N, 256>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x - kFirstEpiWarp * 32,
+                                staged, abort_flag);
+    } else {                   // every warp selects, then fills
+      fused_topk<NEXT_N, kThreadsTc>(p, pt, smem + L.k, (int)(L.sc - L.k), (int)threadIdx.x, staged, abort_flag);
+    }
+    run_fill();
   } else {
-    run_fill(false);
+    run_fill();
   }
 
   // ---- tear-down ----------------------------------------------------------------
@@ -1027,6 +1133,20 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, K::TMEM_COLS);
+  }
+  if constexpr (FUSED) {
+    // The last CTA out resets the ready queue's head, tail and done count
+    // and the fill counter: every CTA has taken its last row and unit by then.
+    if (threadIdx.x == 0) {
+      int32_t* qctl = p.req_counter + 5 * (int64_t)p.batch;
+      __threadfence();
+      if (atomicAdd(&qctl[2], 1) == (int)gridDim.x - 1) {
+        qctl[0] = 0;
+        qctl[1] = 0;
+        qctl[2] = 0;
+        qctl[3] = 0;
+      }
+    }
   }
 }
 

@@ -33,6 +33,13 @@ __device__ __forceinline__ void count_if(uint32_t* word, bool pred) {
       :: "r"(a), "r"((uint32_t)pred) : "memory");
 }
 
+// Zero `words` words (a multiple of 4) at a 16-byte aligned shared address.
+template <int NT>
+__device__ __forceinline__ void zero_words(uint32_t* p, int words, int tid) {
+  uint4* v = reinterpret_cast<uint4*>(p);
+  for (int i = tid; i < words / 4; i += NT) v[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 struct SelectResult {
   uint32_t prefix;     // digits chosen so far
   uint32_t mask;       // bits those digits cover
@@ -70,7 +77,7 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* h1 = hist;                              // pass 1: [bin][lane]; pass 3: plain, reused
   uint32_t* h2 = hist + kSelBins1 * 32;             // pass 2: plain
-  for (int i = tid; i < kSelBins1 * 32 + kSelBins2; i += NT) hist[i] = 0;
+  zero_words<NT>(hist, kSelBins1 * 32 + kSelBins2, tid);
   bar();
   SelectResult s{0u, 0u, k};
 #pragma unroll 1
@@ -78,8 +85,7 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
     const int shift = pass == 0 ? 24 : (pass == 1 ? 12 : 0);
     const int nb = pass == 0 ? kSelBins1 : kSelBins2;
     uint32_t* h = pass == 1 ? h2 : h1;
-    if (pass == 1)                                  // pass 3 reuses h1, free since pass 1's search
-      for (int i = tid; i < kSelBins2; i += NT) h1[i] = 0;
+    if (pass == 1) zero_words<NT>(h1, kSelBins2, tid);   // pass 3 reuses h1, free since pass 1's search
     const uint32_t prefix = s.prefix, mask = s.mask;
     if (pass == 0) {
       for_each([&](bool valid, uint32_t key) { count_if(&h1[(key >> 24) * 32 + lane], valid); });
@@ -328,7 +334,7 @@ __device__ __forceinline__ uint32_t* stage_keys(const float* row, int n, uint32_
   const float4* v = reinterpret_cast<const float4*>(row + head);
   uint4* kv = reinterpret_cast<uint4*>(keys + head);
   const int nv = (n - head) >> 2;
-  constexpr int kU = 4;
+  constexpr int kU = 8;
   for (int b = 0; b < nv; b += NT * kU) {
     float4 x[kU];
 #pragma unroll

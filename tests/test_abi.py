@@ -137,7 +137,7 @@ def test_topk_argument_validation(lib, kw, code):
 def _fused(lib, **kw):
     args = dict(q=A16, kv=A16, num_pages=20, page_size=16, weights=A16, ctx=A4, bt=A4, bt_stride=20,
                 batch=2, next_n=1, heads=64, head_dim=128, logits=A4, stride=512, W=512, k=64, idx=A4,
-                idx_stride=64, ws=A4, ws_bytes=8, status=None)
+                idx_stride=64, ws=A4, ws_bytes=4 * (5 * 2 + 4), status=None)
     args.update(kw)
     return lib.sai_paged_mqa_logits_topk(
         args["q"], args["kv"], args["num_pages"], args["page_size"], args["weights"], args["ctx"],
@@ -160,8 +160,8 @@ def _fused(lib, **kw):
     (dict(idx=A4 + 2), sai.ERR_MISALIGNED),
     (dict(ws=A4 + 1), sai.ERR_MISALIGNED),
     (dict(ws=None), sai.ERR_WORKSPACE),
-    (dict(ws_bytes=7), sai.ERR_WORKSPACE),
-    (dict(batch=0, ws_bytes=0), sai.OK),
+    (dict(ws_bytes=4 * (5 * 2 + 4) - 1), sai.ERR_WORKSPACE),
+    (dict(batch=0, ws=None, ws_bytes=0), sai.OK),
 ])
 def test_fused_argument_validation(lib, kw, code):
     assert _fused(lib, **kw) == code
@@ -225,7 +225,9 @@ def test_workspace_query(lib):
     n = lib.sai_top_k_workspace_bytes(1024, 32768, 2048)
     assert n >= 0
     assert lib.sai_top_k_workspace_bytes(-1, 10, 10) == 0
-    assert lib.sai_paged_mqa_logits_topk_workspace_bytes(1000) == 4000
+    # a tile counter per request, a queue of four rows per request, head, tail, done
+    assert lib.sai_paged_mqa_logits_topk_workspace_bytes(1000) == 4 * (5 * 1000 + 4)
+    assert lib.sai_paged_mqa_logits_topk_workspace_bytes(0) == 0
     assert lib.sai_paged_mqa_logits_topk_workspace_bytes(-1) == 0
 
 

@@ -30,7 +30,8 @@ def run_fused(w, dev, k=None, workspace=None, status=None):
     logits = torch.full((w.rows, w.logits_stride), 4321.0, dtype=torch.float32, device="cuda")
     idx = torch.full((w.rows, k + 2), -7, dtype=torch.int32, device="cuda")
     if workspace is None:
-        workspace = torch.zeros(max(1, w.batch), dtype=torch.int32, device="cuda")
+        workspace = torch.zeros(max(1, sai.logits_topk_workspace_bytes(w.batch) // 4), dtype=torch.int32,
+                                device="cuda")
     sai.paged_mqa_logits_topk(dev["q"], dev["kv"], w.page_size, dev["weights"], dev["context_lens"],
                               dev["block_table"], logits, w.max_model_len, k, idx[:, :k], workspace,
                               num_pages=w.pool.num_pages, status=status)
@@ -130,7 +131,7 @@ def test_context_clamped_to_table():
 def test_workspace_too_small_is_rejected():
     w = synth.tiny()
     dev = w.to_device()
-    ws = torch.zeros(1, dtype=torch.int32, device="cuda")        # batch 2 needs 8 bytes
+    ws = torch.zeros(12, dtype=torch.int32, device="cuda")       # batch 2 needs 13 words
     with pytest.raises(sai.SaiError) as e:
         run_fused(w, dev, workspace=ws)
     assert e.value.code == sai.ERR_WORKSPACE

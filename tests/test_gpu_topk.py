@@ -218,7 +218,7 @@ def test_wide_fused_rows_past_2g():
     dev = w.to_device()
     logits = torch.full((w.rows, w.logits_stride), 4321.0, dtype=torch.float32, device="cuda")
     idx = torch.full((w.rows, w.topk), -7, dtype=torch.int32, device="cuda")
-    ws = torch.zeros(w.batch, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sai.logits_topk_workspace_bytes(w.batch) // 4, dtype=torch.int32, device="cuda")
     sai.paged_mqa_logits_topk(dev["q"], dev["kv"], w.page_size, dev["weights"], dev["context_lens"],
                               dev["block_table"], logits, w.max_model_len, w.topk, idx, ws,
                               num_pages=w.pool.num_pages)

@@ -61,7 +61,7 @@ def test_two_calls_match_the_workspace_entry_point(name):
     stream = torch.cuda.current_stream().cuda_stream
     ref_logits = torch.empty((w.rows, w.logits_stride), dtype=torch.float32, device="cuda")
     ref_idx = torch.full((w.rows, k), -7, dtype=torch.int32, device="cuda")
-    ws = torch.zeros(w.batch, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sai.logits_topk_workspace_bytes(w.batch) // 4, dtype=torch.int32, device="cuda")
     assert _call_workspace(lib, w, dev, ref_logits, ref_idx, k, ws, stream) == sai.OK
     torch.cuda.synchronize()
     W = w.max_model_len
