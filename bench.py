@@ -90,6 +90,20 @@ def topk_bytes(w) -> int:
     return row_tokens(w) * 4 + w.rows * w.topk * 4
 
 
+TILE_TOKENS, FILL_COLS = 128, 4096     # the logits kernel's MMA tile and -inf fill unit
+
+
+def fill_heavy(w) -> bool:
+    """The logits kernel's rule for a launch whose -inf fill outweighs its
+    tiles four times over (fill units of 4096 columns against 128-token
+    tiles); the fused launch then shares the fill over the whole grid."""
+    ce = np.clip(np.asarray(w.context_lens, dtype=np.int64), 0, w.max_model_len)
+    tiles = (ce + TILE_TOKENS - 1) // TILE_TOKENS
+    fs = np.minimum(w.max_model_len, tiles * TILE_TOKENS)
+    units = w.next_n * ((w.max_model_len - fs + FILL_COLS - 1) // FILL_COLS)
+    return int(units.sum()) > 4 * int(tiles.sum())
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -288,7 +302,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    fused = args.path == "fused"
+    fused = args.path == "fused" or (args.path == "auto" and fill_heavy(w))
 
     def logits_call(d):
         sai.paged_mqa_logits(d["q"], d["kv"], w.page_size, d["weights"], d["context_lens"],
@@ -554,7 +568,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "ms_per_step_mean": ms_mean / K,
                        "ms_per_step_min_max": [min(meas) / K, max(meas) / K],
                        "path": ("one fused launch (logits; rows of completed requests queued and selected by "
-                                "every CTA while its other warps write the -inf fill)"
+                                "every CTA while its other warps write the -inf fill"
+                                + (", fill units shared by the whole grid through one counter)"
+                                   if fill_heavy(w) else ")")
                                 if fused else "two launches (logits, top-k)"),
                        "logits_ms": lg_ms, "topk_ms": None if fused else tk_ms,
                        "logits_ms_median": float(np.median(logits_ms)),
@@ -944,13 +960,17 @@ def main():
     ap.add_argument("--sweep", default=None,
                     help="run the throughput sweep instead: 'subset' (every P, next_n, H at B in {64, 256}, "
                          "ctx in {8192, 65536}), 'all' (600 points) or 'P,n,H,B,ctx;...'")
-    ap.add_argument("--path", choices=["fused", "separate"], default="separate",
-                    help="one fused logits + top-k launch per step, or the two launches")
+    ap.add_argument("--path", choices=["auto", "fused", "separate"], default="auto",
+                    help="one fused logits + top-k launch per step, or the two launches; auto: fused "
+                         "where the -inf fill outweighs the logits tiles four times over (the wide "
+                         "workload), where the fused launch spreads the fill over the whole grid")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.path == "fused" and args.layout != "split":
         ap.error("the fused logits + top-k launch reads page-split caches only")
+    if args.path == "auto" and args.layout != "split":
+        args.path = "separate"
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
