@@ -103,6 +103,20 @@ def test_many_small_requests():
     _check(w, k=64, oracle=False)
 
 
+@pytest.mark.parametrize("next_n,heads", [(1, 64), (4, 64), (2, 128)])
+def test_fill_heavy_launch(next_n, heads):
+    # The -inf fill outweighs the tiles four times over: every CTA takes fill
+    # units from the workspace's grid-wide counter, and the epilogue warps
+    # select rows while the other warps fill.  Rows shorter than k (written
+    # by the CTA that completes their request), rows longer than k (through
+    # the ready queue), an empty request, and a width that is not a multiple
+    # of the 4096-column fill unit, with a padded row stride.
+    ctx = [0, 1, 127, 128, 129, 2047, 2048, 2049, 2050, 3000, 4500, 130, 2100, 3, 2600, 3777]
+    w = synth.custom(batch=16, next_n=next_n, heads=heads, page_size=16, context_lens=ctx,
+                     max_model_len=400000, logits_stride=400128, topk=2048, seed=40 + next_n + heads)
+    _check(w, k=2048)
+
+
 def test_all_contexts_empty():
     w = synth.custom(batch=5, next_n=2, heads=64, page_size=16, context_lens=[0, 0, 0, 0, 0],
                      max_model_len=256, seed=3)

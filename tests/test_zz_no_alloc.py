@@ -48,14 +48,22 @@ def test_batch_beyond_the_static_counters_is_rejected():
     assert rc == sai.ERR_INVALID_ARGUMENT
 
 
+def _fill_heavy():
+    # -inf fill four times the tiles: the grid-wide fill counter (the static
+    # array's word after the queue's head, tail and done count) is used.
+    return synth.custom(batch=16, next_n=2, heads=64, page_size=16,
+                        context_lens=[0, 1, 127, 2049, 3000, 130, 4100, 3, 2600, 3777, 4500, 128, 2047, 1, 300, 64],
+                        max_model_len=400000, logits_stride=400128, topk=2048, seed=77)
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "decode", "mtp"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "mtp", "fill_heavy"])
 def test_two_calls_match_the_workspace_entry_point(name):
     import torch
 
     sai.build()
     lib = sai.library()
-    w = {"tiny": synth.tiny, "decode": synth.decode, "mtp": synth.mtp}[name]()
+    w = {"tiny": synth.tiny, "decode": synth.decode, "mtp": synth.mtp, "fill_heavy": _fill_heavy}[name]()
     dev = w.to_device()
     k = w.topk
     stream = torch.cuda.current_stream().cuda_stream
