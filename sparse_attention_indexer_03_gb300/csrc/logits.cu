@@ -548,8 +548,7 @@ __device__ void fused_topk(const TcParams& p, const Part& pt, uint8_t* ring, int
     int32_t* out = p.indices + (int64_t)row * p.idx_stride;  // 64-bit row base
     const float* lrow = p.logits + (int64_t)row * p.stride;
     if (n <= key_cap) {
-      const uint32_t* keys = stage_keys<NT>(lrow, (int)n, key_base, etid);
-      topk_row_smem<NT>(keys, (int)n, k, out, *sh, hist, etid, ebar);
+      topk_row_staged<NT>(lrow, (int)n, k, out, *sh, hist, key_base, etid, ebar);
     } else {
       topk_row_stream<NT>(lrow, n, k, out, *sh, hist, etid, ebar);
     }

@@ -26,11 +26,14 @@ constexpr size_t kSelectSmem = (size_t)(kSelBins1 * 32 + kSelBins2) * sizeof(uin
 
 // Shared-memory add of 1 under a predicate, as one predicated instruction:
 // lanes whose key is outside the bin issue nothing and no branch is formed.
+// No memory clobber: the compiler may issue later keys' loads before the
+// adds; the group barrier that ends a count (a volatile asm with a memory
+// clobber) keeps every add before every read of the bins.
 __device__ __forceinline__ void count_if(uint32_t* word, bool pred) {
   const uint32_t a = (uint32_t)__cvta_generic_to_shared(word);
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p red.shared.add.u32 [%0], 1;\n\t}"
-      :: "r"(a), "r"((uint32_t)pred) : "memory");
+      :: "r"(a), "r"((uint32_t)pred));
 }
 
 // Zero `words` words (a multiple of 4) at a 16-byte aligned shared address.
@@ -69,16 +72,20 @@ struct LocalCounts {
 // `row_counts(pass, cnt, per, wbase, lane)` turns the counts of the bins a
 // thread owns (bin wbase + 32 * i + lane in cnt[i], i < per) into the whole
 // row's, for rows split over several groups; every group then takes the
-// same digits.
+// same digits.  With `first_counted` the caller has zeroed `hist` and
+// counted pass 1 itself (count_first below), and a barrier has followed.
 template <int NT, typename Bar, typename ForEach, typename RowCounts = LocalCounts>
 __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint32_t* hist, uint32_t k, int tid,
-                                                     Bar bar, ForEach for_each, RowCounts row_counts = {}) {
+                                                     Bar bar, ForEach for_each, RowCounts row_counts = {},
+                                                     bool first_counted = false) {
   constexpr int kW = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* h1 = hist;                              // pass 1: [bin][lane]; pass 3: plain, reused
   uint32_t* h2 = hist + kSelBins1 * 32;             // pass 2: plain
-  zero_words<NT>(hist, kSelBins1 * 32 + kSelBins2, tid);
-  bar();
+  if (!first_counted) {
+    zero_words<NT>(hist, kSelBins1 * 32 + kSelBins2, tid);
+    bar();
+  }
   SelectResult s{0u, 0u, k};
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
@@ -88,13 +95,14 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
     if (pass == 1) zero_words<NT>(h1, kSelBins2, tid);   // pass 3 reuses h1, free since pass 1's search
     const uint32_t prefix = s.prefix, mask = s.mask;
     if (pass == 0) {
-      for_each([&](bool valid, uint32_t key) { count_if(&h1[(key >> 24) * 32 + lane], valid); });
+      if (!first_counted)
+        for_each([&](bool valid, uint32_t key) { count_if(&h1[(key >> 24) * 32 + lane], valid); });
     } else {
       for_each([&](bool valid, uint32_t key) {
         count_if(&h[(key >> shift) & (uint32_t)(nb - 1)], valid && (key & mask) == prefix);
       });
     }
-    bar();
+    if (pass != 0 || !first_counted) bar();
     // Thread (warp w, lane l) owns bins w * 32 * per + 32 * i + l, i < per:
     // a warp reads rows of 32 consecutive bins, one per bank.  Bins past nb
     // count zero.
@@ -277,18 +285,6 @@ struct RegRun {
   }
 };
 
-// Keys of a lane's run in shared memory: keys[base + i], i < len, read at
-// min(base + i, n - 1) so the reads stay inside the n staged keys.
-struct SmemRun {
-  const uint32_t* keys;
-  int base, len, n;
-  template <typename F>
-  __device__ __forceinline__ void for_each(F&& f) const {
-#pragma unroll 4
-    for (int i = 0; i < len; ++i) f(i, keys[min(base + i, n - 1)]);
-  }
-};
-
 // Top-k of one row read from global memory (through L2: written by other
 // CTAs of the same launch, or by an earlier kernel).  Row length n > k.
 // The radix passes read the row as 16-byte vectors, consecutive threads on
@@ -322,15 +318,33 @@ __device__ __forceinline__ void topk_row_stream(const float* row, int64_t n, int
   compact_stream<NT>(sh, s, n, k, out, tid, bar, [&](int64_t i) { return float_key(__ldcg(row + i)); });
 }
 
-// Keys of row[0, n) copied into shared memory: key of column c at keys[c].
-// `keys` must have room for n + 3 words past `base`; the returned pointer is
-// `base` shifted by 0..3 words so that 16-byte row segments land on 16-byte
-// shared addresses.  No barrier: the caller's next group barrier publishes it.
+// A row's keys staged in shared memory: key of column c at keys[c]; keys +
+// head is 16-byte aligned, so columns [head, head + 4 nv) are nv 16-byte
+// vectors and [head + 4 nv, n) a scalar tail of at most 3 (head <= 3 too).
+struct StagedRow {
+  const uint32_t* keys;
+  int n, head, nv;
+  __device__ __forceinline__ const uint4* vec() const { return reinterpret_cast<const uint4*>(keys + head); }
+  __device__ __forceinline__ int tail0() const { return head + 4 * nv; }
+};
+
+// Copies row[0, n) into shared memory as keys (16-byte loads from L2, eight
+// in flight per thread, consecutive threads on consecutive vectors) and
+// counts pass 1 of the radix select on the way: `hist` must be zero and a
+// barrier must separate this from the select.  `base` needs room for n + 3
+// words; the keys start 0..3 words past it so that 16-byte row segments
+// land on 16-byte shared addresses.
 template <int NT>
-__device__ __forceinline__ uint32_t* stage_keys(const float* row, int n, uint32_t* base, int tid) {
+__device__ __forceinline__ StagedRow stage_and_count(const float* row, int n, uint32_t* base, uint32_t* hist,
+                                                     int tid) {
+  const int lane = tid & 31;
   const int head = min(n, (int)(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 2));
   uint32_t* keys = base + ((4 - head) & 3);
-  if (tid < head) keys[tid] = float_key(__ldcg(row + tid));
+  auto put = [&](int c, uint32_t key) {
+    keys[c] = key;
+    count_if(&hist[(key >> 24) * 32 + lane], true);
+  };
+  if (tid < head) put(tid, float_key(__ldcg(row + tid)));
   const float4* v = reinterpret_cast<const float4*>(row + head);
   uint4* kv = reinterpret_cast<uint4*>(keys + head);
   const int nv = (n - head) >> 2;
@@ -345,25 +359,75 @@ __device__ __forceinline__ uint32_t* stage_keys(const float* row, int n, uint32_
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int i = b + u * NT + tid;
-      if (i < nv) kv[i] = make_uint4(float_key(x[u].x), float_key(x[u].y), float_key(x[u].z), float_key(x[u].w));
+      if (i < nv) {
+        const uint4 k4 = make_uint4(float_key(x[u].x), float_key(x[u].y), float_key(x[u].z), float_key(x[u].w));
+        kv[i] = k4;
+        count_if(&hist[(k4.x >> 24) * 32 + lane], true);
+        count_if(&hist[(k4.y >> 24) * 32 + lane], true);
+        count_if(&hist[(k4.z >> 24) * 32 + lane], true);
+        count_if(&hist[(k4.w >> 24) * 32 + lane], true);
+      }
     }
   }
-  for (int i = head + nv * 4 + tid; i < n; i += NT) keys[i] = float_key(__ldcg(row + i));
-  return keys;
+  for (int i = head + nv * 4 + tid; i < n; i += NT) put(i, float_key(__ldcg(row + i)));
+  return StagedRow{keys, n, head, nv};
 }
 
-// Top-k of a row whose keys are in shared memory (stage_keys).  Row length
-// n > k.  Each lane owns a run of len consecutive columns, len odd so that
-// the 32 lanes of a warp read 32 different banks.
+// Every key of a staged row once, in no particular order (the radix passes'
+// counts): thread t reads vectors t, t + NT, ... (consecutive threads on
+// consecutive 16-byte vectors: four keys per load, no bank conflict), four
+// loads ahead of their adds, then the scalar head and tail.
+template <int NT, typename F>
+__device__ __forceinline__ void staged_for_each(const StagedRow& r, int tid, F&& f) {
+  const uint4* kv = r.vec();
+  constexpr int kU = 4;
+  for (int b = tid; b < r.nv; b += NT * kU) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) x[u] = kv[min(b + u * NT, r.nv - 1)];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const bool v = b + u * NT < r.nv;
+      f(v, x[u].x);
+      f(v, x[u].y);
+      f(v, x[u].z);
+      f(v, x[u].w);
+    }
+  }
+  if (tid < r.head) f(true, r.keys[tid]);
+  if (tid < r.n - r.tail0()) f(true, r.keys[r.tail0() + tid]);
+}
+
+// Keys of a lane's run in shared memory: keys[base + i], i < len, read at
+// min(base + i, n - 1) so the reads stay inside the n staged keys (the
+// ordered compaction of a staged row).
+struct SmemRun {
+  const uint32_t* keys;
+  int base, len, n;
+  template <typename F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+#pragma unroll 4
+    for (int i = 0; i < len; ++i) f(i, keys[min(base + i, n - 1)]);
+  }
+};
+
+// Top-k of row[0, n) (n > k), staged into shared memory at `key_base` (room
+// for n + 3 words) with pass 1 counted on the way.
 template <int NT, typename Bar>
-__device__ __forceinline__ void topk_row_smem(const uint32_t* keys, int n, int k, int32_t* out,
-                                              SelectShared<NT>& sh, uint32_t* hist, int tid, Bar bar) {
+__device__ __forceinline__ void topk_row_staged(const float* row, int n, int k, int32_t* out, SelectShared<NT>& sh,
+                                                uint32_t* hist, uint32_t* key_base, int tid, Bar bar) {
+  zero_words<NT>(hist, kSelBins1 * 32 + kSelBins2, tid);
+  bar();
+  const StagedRow r = stage_and_count<NT>(row, n, key_base, hist, tid);
+  bar();
+  auto for_each = [&](auto&& f) { staged_for_each<NT>(r, tid, f); };
+  const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each, LocalCounts{}, true);
+  // The compaction by lane runs: lane l of warp w owns about n / NT
+  // consecutive columns from (w * 32 + l) * len (len odd: the 32 lanes'
+  // reads fall in 32 banks).
   const int len = ((n + NT - 1) / NT) | 1;
   const int base = (tid >> 5) * 32 * len + (tid & 31) * len;
-  const SmemRun run{keys, base, len, n};
-  auto for_each = [&](auto&& f) { run.for_each([&](int i, uint32_t key) { f(base + i < n, key); }); };
-  const SelectResult s = radix_select<NT>(sh, hist, (uint32_t)k, tid, bar, for_each);
-  compact_lanes<NT>(sh, s, n, k, out, tid, bar, base, len, run);
+  compact_lanes<NT>(sh, s, n, k, out, tid, bar, base, len, SmemRun{r.keys, base, len, n});
 }
 
 }  // namespace sai

@@ -206,8 +206,9 @@ topk_cluster_kernel(TopKArgs a) {
 }
 
 // ---- wider rows: a row of up to KEYS columns has its keys copied into
-// shared memory once its length is known (each lane then a run of about
-// n / NT columns); a longer row is re-read from L2 on every pass.  For
+// shared memory once its length is known (the radix passes then read them
+// as 16-byte vectors; pass 1 is counted during the copy); a longer row is
+// re-read from L2 on every pass.  For
 // logical widths up to 40960, one CTA of 1024 threads per SM stages every
 // row.  Wider rows (the wide outputs, whose rows hold far fewer context
 // columns than their width) go to CTAs of 512 threads staging up to 16384
@@ -231,8 +232,7 @@ topk_smem_kernel(TopKArgs a) {
   const float* row = a.logits + r * a.stride;
   if (n <= KEYS) {
     uint32_t* key_base = reinterpret_cast<uint32_t*>(topk_smem + kSelectSmem);
-    const uint32_t* keys = stage_keys<NT>(row, (int)n, key_base, threadIdx.x);
-    topk_row_smem<NT>(keys, (int)n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
+    topk_row_staged<NT>(row, (int)n, a.k, out, sh, hist, key_base, threadIdx.x, CtaBar{});
   } else {
     topk_row_stream<NT>(row, n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
   }
