@@ -38,7 +38,7 @@ def run_fused(w, dev, k=None, workspace=None, status=None):
     return logits, idx, workspace
 
 
-def _check(w, k=None, oracle=True, repeat=True):
+def _check(w, k=None, oracle=True, repeat=True, sample=None):
     k = k or w.topk
     W = w.max_model_len
     dev = w.to_device()
@@ -57,6 +57,10 @@ def _check(w, k=None, oracle=True, repeat=True):
         ref = oracle_logits(w)
         assert_logits_close(logits[:, :W].cpu().numpy(), ref, "fused logits")
         assert_topk_valid(idx[:, :k].cpu().numpy(), ref, row_ctx(w), k, "fused top-k")
+    if sample is not None:                            # the oracle on sampled rows only
+        ref = oracle_logits(w, rows=sample)
+        assert_logits_close(logits[sample, :W].cpu().numpy(), ref, "fused logits (sampled rows)")
+        assert_topk_valid(idx[sample, :k].cpu().numpy(), ref, row_ctx(w)[sample], k, "fused top-k (sampled rows)")
     if repeat:
         logits2, idx2, _ = run_fused(w, dev, k, workspace=ws)
         torch.cuda.synchronize()
@@ -71,9 +75,23 @@ def test_decode():
     _check(synth.decode())
 
 
+def _mtp_sample(w, count=48):
+    """Rows of the MTP batch for the oracle: the longest rows, the empty
+    request's, rows just past and just below k, and random ones."""
+    n_r = row_ctx(w)
+    order = np.argsort(-n_r, kind="stable")
+    near_k = np.argsort(np.abs(n_r - w.topk), kind="stable")[:8]
+    empty = np.flatnonzero(n_r == 0)[:2]
+    rng = np.random.default_rng(5)
+    rows = set(order[:12].tolist()) | set(near_k.tolist()) | set(empty.tolist())
+    rows |= set(rng.integers(0, w.rows, count).tolist())
+    return sorted(rows)
+
+
 @pytest.mark.slow
 def test_mtp():
-    _check(synth.mtp(), oracle=False)
+    w = synth.mtp()
+    _check(w, oracle=False, sample=_mtp_sample(w))
 
 
 @pytest.mark.parametrize("next_n,heads", [(1, 64), (2, 128), (3, 64), (3, 128), (4, 64), (4, 128)])
@@ -100,7 +118,7 @@ def test_many_small_requests():
     ctx[::50] = 0
     w = synth.custom(batch=700, next_n=1, heads=64, page_size=16, context_lens=ctx, max_model_len=512,
                      seed=7)
-    _check(w, k=64, oracle=False)
+    _check(w, k=64)
 
 
 @pytest.mark.parametrize("next_n,heads", [(1, 64), (4, 64), (2, 128)])

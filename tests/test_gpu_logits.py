@@ -166,10 +166,16 @@ def test_wide_rows_past_2g():
     n_r = torch.from_numpy(row_ctx(w)).cuda()
     assert torch.equal(torch.isfinite(view).sum(dim=1), n_r)
     assert torch.equal((view == -np.inf).sum(dim=1), w.max_model_len - n_r)
+    # Sampled rows against the oracle over every finite column and 256 -inf
+    # ones past the longest: the rows around the 2^31-byte boundary, both
+    # ends, one row in every block of 32 (a row of each of the 32 row blocks
+    # the CTAs' work splits into, roughly), and random ones.
     rng = np.random.default_rng(0)
-    sample = sorted(set([0, 1, 510, 511, 512, 513, 767, 1022, 1023] + rng.integers(0, 1024, 12).tolist()))
+    sample = set([0, 1, 510, 511, 512, 513, 767, 1022, 1023] + rng.integers(0, 1024, 24).tolist())
+    sample |= set((np.arange(32) * 32 + rng.integers(0, 32, 32)).tolist())
+    sample = sorted(sample)
     wmax = int(row_ctx(w)[sample].max()) + 256
-    ref = oracle_logits(w, rows=sample, W=w.max_model_len)[:, :wmax]
+    ref = oracle_logits(w, rows=sample, W=wmax)
     assert_logits_close(view[sample, :wmax].cpu().numpy(), ref)
 
 
