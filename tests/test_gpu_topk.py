@@ -100,6 +100,26 @@ def test_long_rows(W):
     assert_topk_exact(got, vals, n_r, k)
 
 
+@pytest.mark.parametrize("batch,next_n,W", [(300, 3, 32768), (1100, 1, 20000), (400, 2, 100000)])
+def test_many_rows_longest_first(batch, next_n, W):
+    # More rows than one wave of CTAs, on both shared-memory kernels (one CTA
+    # of 1024 threads per SM up to 40960 columns, two of 512 beyond, where
+    # rows longer than 16384 columns are re-read from L2 on each pass): the
+    # same sets as the oracle's top-k on the same values, and 0..n-1 then -1
+    # for the short rows.  Contexts span empty to the full width and repeat.
+    rng = np.random.default_rng(batch + W)
+    k = 2048
+    ctx = np.exp(rng.uniform(0, np.log(W), size=batch)).astype(np.int64)
+    ctx[rng.integers(0, batch, 8)] = 0
+    ctx[rng.integers(0, batch, 8)] = W
+    ctx[:20] = ctx[20:40]                                  # equal contexts in different places
+    rows = batch * next_n
+    vals = rng.standard_normal((rows, W)).astype(np.float32)
+    got = _run_on_values(vals, ctx, next_n, k, W)
+    n_r = np.clip(np.repeat(ctx, next_n) - next_n + np.tile(np.arange(next_n), batch) + 1, 0, W)
+    assert_topk_exact(got, vals, n_r, k)
+
+
 def _ties_order(v: np.ndarray, n: int, k: int) -> np.ndarray:
     """Expected entries of a row whose values near the k-th largest are exact
     ties: the columns above the k-th largest value ascending, then the lowest
