@@ -143,7 +143,7 @@ struct Cfg {
   // K ring depth: as many 128-token stages as fit beside two Q slots (at
   // most 8), with as many producer warps (3, else 2) as keep the ring's
   // parity waits sound.
-  static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 1) + 64 +
+  static constexpr int FIXED = 1024 + 2 * Q_BYTES + kProducers * kLookahead * 32 * 4 + 8 * (4 + 2 * ACC + 2) + 64 +
                                kCtxSmem * 4;
   static constexpr int STAGE_BYTES = IL ? kStageBytesIl : kStageBytes;
   // The tile's head weights [next_n, H] fp32 come into the stage with its K
@@ -153,9 +153,16 @@ struct Cfg {
   static constexpr int W_BYTES = STAGE_W ? NEXT_N * H * 4 : 0;
   static constexpr int PER_STAGE = STAGE_BYTES + kScaleSlot + 16 + 16 + (IL ? 8 : 0) + W_BYTES;
   static constexpr int FIT = (kMaxSmem - FIXED) / PER_STAGE < 8 ? (kMaxSmem - FIXED) / PER_STAGE : 8;
-  static constexpr int PRODUCERS = ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2;
+  // Tiles of one job of at most 128 columns (decode-like shapes: the MMA
+  // warp's per-tile loop, not the tensor pipe, sets the tile rate): two MMA
+  // warps take alternate tiles (warp kMmaWarp the even ones, warp 2 the odd
+  // ones), each with its own two of the four accumulators, fed by two
+  // producer warps.  An even ring gives every stage to one MMA warp.
+  static constexpr bool DUAL = !IL && C == 1 && N <= 128;
+  static constexpr int PRODUCERS = DUAL ? 2 : (ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2);
   static constexpr int STAGES = deepest_sound_ring(FIT, PRODUCERS, C);
   static_assert(STAGES >= 2 && ring_waits_unambiguous(STAGES, PRODUCERS, C), "shared memory");
+  static_assert(!DUAL || (STAGES % 2 == 0 && ACC % 2 == 0 && kMmaWarp == 3), "two MMA warps");
   static_assert(N % QBOX == 0 && NC % 16 == 0 && NC <= 256 && ACC * NC <= 512, "shape");
 };
 
@@ -179,7 +186,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int q_bytes, int a
   L.wst = L.meta + stages * 16;                        // per-stage head weights (w_bytes each, may be 0)
   L.ids = L.wst + stages * w_bytes;
   L.bar = L.ids + kProducers * kLookahead * 32 * 4;
-  L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 1 + (il ? stages : 0));
+  L.misc = L.bar + 8 * (2 * stages + 4 + 2 * acc + 2 + (il ? stages : 0));
   L.ctx = L.misc + 64;
   L.total = L.ctx + kCtxSmem * 4;
   return L;
@@ -379,6 +386,32 @@ struct Cursor {
       load(p, cc, lane);
     } while (nt == 0 && b + 1 < p.batch);
     return 1;
+  }
+};
+
+// The same walk for one thread (no warp shuffles), counting the requests
+// entered: q is the Q load index of the current tile's request.
+struct ScalarCursor {
+  int b = 0, t = 0, q = 0;
+  int64_t nt = 0;
+  const int32_t* staged = nullptr;
+  __device__ __forceinline__ void load(const TcParams& p) {
+    nt = req_tiles(ctx_eff(staged ? staged[b] : p.context_lens[b], p.cap));
+  }
+  __device__ __forceinline__ void start(const TcParams& p, int b0, int t0) {
+    b = b0;
+    t = t0;
+    q = 0;
+    load(p);
+  }
+  __device__ __forceinline__ void advance(const TcParams& p) {
+    if (++t < nt) return;
+    t = 0;
+    do {
+      ++b;
+      load(p);
+    } while (nt == 0 && b + 1 < p.batch);
+    ++q;
   }
 };
 
@@ -663,8 +696,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
   auto qempty = [&](int q) { return bar + 8u * (2 * stages + 2 + q); };
   auto tfull = [&](int a) { return bar + 8u * (2 * stages + 4 + a); };
   auto tempty = [&](int a) { return bar + 8u * (2 * stages + 4 + K::ACC + a); };
-  const uint32_t drain = bar + 8u * (2 * stages + 4 + 2 * K::ACC);
-  auto stgbar = [&](int s) { return bar + 8u * (2 * stages + 4 + 2 * K::ACC + 1 + s); };   // IL staging
+  const uint32_t drain = bar + 8u * (2 * stages + 4 + 2 * K::ACC);       // [0] MMA warp, [1] the second one
+  auto stgbar = [&](int s) { return bar + 8u * (2 * stages + 4 + 2 * K::ACC + 2 + s); };   // IL staging
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   int* fill_next = reinterpret_cast<int*>(smem + L.misc + 8);      // next -inf fill unit to take
@@ -697,13 +730,14 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
       for (int q = 0; q < 2; ++q) {
         ptx::mbar_init(qfull(q), 1);
-        ptx::mbar_init(qempty(q), 1);
+        ptx::mbar_init(qempty(q), K::DUAL ? 2 : 1);    // each MMA warp commits every Q load's release
       }
       for (int a = 0; a < K::ACC; ++a) {
         ptx::mbar_init(tfull(a), 1);
         ptx::mbar_init(tempty(a), 4);
       }
       ptx::mbar_init(drain, 1);
+      ptx::mbar_init(drain + 8u, 1);
       if constexpr (IL)
         for (int s = 0; s < stages; ++s) ptx::mbar_init(stgbar(s), 1);
       *abort_flag = 0;
@@ -756,6 +790,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
     // Warp 0 alone loads Q, for every request in order as its cursor crosses
     // request starts (its own tiles' and the other warps'): waiting on a Q
     // slot's release in sequence keeps each parity wait unambiguous.
+    const bool q_here = pw == 0;
     CtxCache cc, cc_la;
     cc.staged = cc_la.staged = staged;
     Cursor cur, la;
@@ -780,11 +815,11 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const int entered = cur.advance(p, cc, lane);
       ++ci;
       q_seq += entered;
-      if (entered && pw == 0 && qok) issue_q(cur.b, q_seq);
+      if (entered && q_here && qok) issue_q(cur.b, q_seq);
     };
     if (own > 0) {
       cur.start(p, pt.b0, pt.t0, cc, lane);
-      if (pw == 0) issue_q(cur.b, 0);
+      if (q_here) issue_q(cur.b, 0);
       for (int x = 0; x < pw; ++x) step();
       la = cur;
     }
@@ -883,7 +918,6 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       const uint32_t ph = (uint32_t)(i / stages) & 1u;
       const bool is_new = (i == 0) || (cur.t == 0);
       const bool is_last = (cur.t == cur.nt - 1) || (i == pt.n_tiles - 1);
-      const int qs = q_seq & 1;
       if (!qok) { ok = false; break; }
       if (!wait_filling(kempty(s), ph ^ 1u)) { ok = false; if (lane == 0) fail(); break; }
       if (j == 0) ptx::cp_async_wait<0>();                    // page ids of this tile have landed
@@ -901,7 +935,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         if (bad) raise_status(p.status, SAI_STATUS_BAD_PAGE);
         if (lane == 0) {
           meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
-                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
+                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (q_seq << 8));
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_expect_tx(stgbar(s), nload * box_bytes + K::W_BYTES);
@@ -935,7 +969,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         }
         if (lane == 0) {
           meta[s] = make_int4(cur.b, cur.t, (int)max((int64_t)INT32_MIN, min((int64_t)INT32_MAX, cur.raw)),
-                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (qs << 8));
+                              (is_new ? kFlagNew : 0) | (is_last ? kFlagLast : 0) | (q_seq << 8));
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_expect_tx(full(s), nload * box_bytes + K::W_BYTES);
@@ -968,7 +1002,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
       }
     }
     // Warp 0 still loads Q for requests that start in the other warps' last tiles.
-    if (pw == 0 && ok && own > 0)
+    if (q_here && ok && own > 0)
       while (ci + 1 < pt.n_tiles && qok) step();
     ok = ok && qok;
     ptx::cp_async_wait<0>();
@@ -981,27 +1015,68 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
         if (k2 % NP == pw)
           ptx::mbar_wait_warp(full(k2 % stages), (uint32_t)(k2 / stages) & 1u, &zero_flag, 1LL << 26);
     }
-  } else if (warp == kMmaWarp) {
-    // ---- MMA issuer -------------------------------------------------------------
+  } else if (warp == kMmaWarp || (K::DUAL && warp == 2)) {
+    // ---- MMA issuer(s) ----------------------------------------------------------
+    // One warp issues every tile; with DUAL, warp kMmaWarp the even tiles and
+    // warp 2 the odd ones.  Tile i's job goes to accumulator i % ACC, which
+    // the epilogue releases in tile order, so the two warps' accumulators
+    // are disjoint.  Q loads (one per request, in order, slot q & 1, issued
+    // by producer warp 0, which waits for each slot's release in order): the
+    // single warp waits for a request's Q at its first tile and releases it
+    // after its last.  Two warps each wait for every Q load in order (also
+    // those of requests whose tiles all went to the other warp), and each
+    // walks the tiles itself (a scalar cursor), so that right after its last
+    // tile of a request, before its next tile has landed, it commits the
+    // release of every load before its next tile's request; a Q slot's
+    // release needs both commits.  (Releasing only on reading the next
+    // tile's request can deadlock: producer warp 0 may be waiting for that
+    // release before it issues that very tile.)  A warp waits for load q only
+    // after load q - 2 has landed and commits load q's release only after
+    // waiting for it, so each parity wait and each arrival is on the phase
+    // it means (simulated in the protocol tests).
+    const int mw = warp == kMmaWarp ? 0 : 1;
+    const uint32_t my_drain = drain + 8u * (uint32_t)mw;
     if (lane == 0) {
-      int q_count = 0, acc_count = 0;
+      int q_count = 0, acc_count = 0;                  // single warp
+      int q_waited = 0, q_done = 0;                    // DUAL: Q loads waited for / released by this warp
+      ScalarCursor sc;                                 // DUAL: at this warp's current tile
+      sc.staged = staged;
+      if (K::DUAL && pt.n_tiles > mw) {
+        sc.start(p, pt.b0, pt.t0);
+        if (mw == 1) sc.advance(p);
+      }
+      // DUAL: wait for load j (in order), then commit its release.
+      auto wait_q = [&](int j) {
+        return ptx::mbar_wait(qfull(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, kWaitBudget);
+      };
       bool aborted = false;
-      for (int i = 0; i < pt.n_tiles; ++i) {
+      for (int i = K::DUAL ? mw : 0; i < pt.n_tiles; i += K::DUAL ? 2 : 1) {
         const int s = i % stages;
+        int qs;
+        if constexpr (K::DUAL) {
+          const int qi = sc.q;                         // this tile's request's Q load
+          bool qok_mma = true;
+          for (; qok_mma && q_waited <= qi; ++q_waited) qok_mma = wait_q(q_waited);
+          if (!qok_mma) { fail(); aborted = true; break; }
+          qs = qi & 1;
+        }
         // The stage and Q barriers are completed by TMA, not by tcgen05
-        // operations, so no tcgen05 fence is needed after these two waits.
+        // operations, so no tcgen05 fence is needed after these waits.
         if (!ptx::mbar_wait(full(s), (uint32_t)(i / stages) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
         const int4 m = meta[s];
-        const int qs = (m.w >> 8) & 1;
-        if (m.w & kFlagNew) {
-          if (!ptx::mbar_wait(qfull(qs), (uint32_t)(q_count >> 1) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
-          ++q_count;
+        if constexpr (!K::DUAL) {
+          qs = (m.w >> 8) & 1;
+          if (m.w & kFlagNew) {
+            if (!ptx::mbar_wait(qfull(qs), (uint32_t)(q_count >> 1) & 1u, abort_flag, kWaitBudget)) { fail(); aborted = true; break; }
+            ++q_count;
+          }
         }
         bool ok = true;
 #pragma unroll 1
         for (int c = 0; c < K::C; ++c, ++acc_count) {
-          const int a = acc_count % K::ACC;
-          if (!ptx::mbar_wait(tempty(a), ((uint32_t)(acc_count / K::ACC) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
+          const int job = K::DUAL ? i : acc_count;     // DUAL: one job per tile
+          const int a = job % K::ACC;
+          if (!ptx::mbar_wait(tempty(a), ((uint32_t)(job / K::ACC) & 1u) ^ 1u, abort_flag, kWaitBudget)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t d = tmem_base + (uint32_t)(a * K::NC);
           const uint64_t adesc = ptx::desc_kmajor_sw128(s_k + s * K::STAGE_BYTES);
@@ -1012,16 +1087,38 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_const
           ptx::mma_commit(tfull(a));
         }
         if (!ok) { fail(); aborted = true; break; }
-        // The stage is released by the epilogue warps of its jobs, each after
-        // its accumulator is complete, hence after every MMA reading the stage.
-        if (m.w & kFlagLast) ptx::mma_commit(qempty(qs));
+        if constexpr (K::DUAL) {
+          // Release the loads before the next own tile's request (all those
+          // waited for, past the last tile).
+          int q_next = sc.q + 1;
+          if (i + 2 < pt.n_tiles) {
+            sc.advance(p);
+            sc.advance(p);
+            q_next = sc.q;
+          }
+          bool qok_mma = true;
+          while (q_done < q_next) {
+            if (q_done == q_waited) {
+              qok_mma = wait_q(q_waited);
+              if (!qok_mma) break;
+              ++q_waited;
+            }
+            ptx::mma_commit(qempty(q_done & 1));
+            ++q_done;
+          }
+          if (!qok_mma) { fail(); aborted = true; break; }
+        } else if (m.w & kFlagLast) {
+          // The stage is released by the epilogue warps of its jobs, each after
+          // its accumulator is complete, hence after every MMA reading the stage.
+          ptx::mma_commit(qempty(qs));
+        }
       }
       // After an abort, the MMAs already issued complete before TMEM is freed
       // (otherwise the epilogue has already seen every one of them complete).
       if (aborted) {
         const int zero_flag = 0;
-        ptx::mma_commit(drain);
-        ptx::mbar_wait(drain, 0, &zero_flag, 1LL << 28);
+        ptx::mma_commit(my_drain);
+        ptx::mbar_wait(my_drain, 0, &zero_flag, 1LL << 28);
       }
     }
     __syncwarp();

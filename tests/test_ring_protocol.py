@@ -120,3 +120,231 @@ def test_holding_with_as_many_stages_as_producers_can_deadlock():
     # waits for the release of tile i + NP - S = i, its own unfinished tile.
     outcomes = {simulate(3, 3, 1, 4, tiles=36, seed=seed, hold=True) for seed in range(200)}
     assert "deadlock" in outcomes, outcomes
+
+
+# ---------------------------------------------------------------- Q slots, two MMA warps
+# With two MMA warps (alternate tiles), Q loads (one per request, in order,
+# slot q & 1) are released by a barrier of count 2: each MMA warp waits for
+# every load in order (also those of requests it has no tile of); at a tile
+# of request q it first commits the release of every load before q (waiting
+# for any of them it has not waited for yet), then waits for the loads up to
+# q; past its last tile it releases the rest it waited for.  The producer issues load q after the release of load
+# q - 2.  Parity waits and counted arrivals are simulated exactly: a wait
+# passes when the barrier's current phase parity differs from the awaited
+# one; an arrival counts toward whatever phase is current.
+
+
+def simulate_q(tile_req, seed, coupled=False, lookahead=False):
+    """tile_req: request index (0, 1, ...) of each tile, non-decreasing, every
+    request present.  Returns 'ok', 'early' (a parity wait passed on a phase
+    other than the awaited one), 'miscount' (an arrival counted toward
+    another load's phase), 'overwrite' (a load reused a slot whose previous
+    request an MMA warp still had tiles of) or 'deadlock'.  A warp reads a
+    tile's request once the tile has landed.  With `coupled`, one producer
+    walks the tiles in order issuing the Q load of each request it enters
+    and the copies of the even tiles, so an even tile lands only after the
+    Q loads of the requests before it were issued; otherwise Q loads and
+    tiles are issued independently.  With `lookahead`, a warp knows the
+    request of its next tile without reading it (it walks the tile
+    sequence itself): once its tile of request r is done and its next tile
+    belongs to a later request q (or it has none), it releases the loads
+    before q (those up to r if it has none), waiting first for any it has
+    not waited for."""
+    rnd = random.Random(seed)
+    n_req = tile_req[-1] + 1
+    full_ph = [0, 0]          # completed phases of qfull[slot] (loads landed in the slot)
+    empty_ph = [0, 0]         # completed phases of qempty[slot]
+    empty_arr = [[], []]      # loads the pending arrivals of qempty[slot] were meant for
+    issued = 0                # loads issued by the producer
+    in_flight = []            # issued, not landed
+    tiles = {w: [i for i in range(len(tile_req)) if i % 2 == w] for w in (0, 1)}
+    pos = {0: 0, 1: 0}        # next tile of each warp
+    waited = {0: 0, 1: 0}     # loads waited for
+    done = {0: 0, 1: 0}       # loads released
+    finished = {0: False, 1: False}
+    walked = 0                # coupled: tiles the producer's walk has passed (and issued, if even)
+
+    def landed(i):
+        return not coupled or i % 2 == 1 or i < walked
+
+    while True:
+        acts = []
+        if issued < n_req:
+            j = issued
+            may = not coupled or (walked < len(tile_req) and tile_req[walked] == j)
+            if may and (j < 2 or (empty_ph[j & 1] & 1) != ((((j - 2) >> 1) & 1))):
+                acts.append(("issue",))
+        if coupled and walked < len(tile_req) and tile_req[walked] < issued:
+            acts.append(("walk",))
+        if in_flight:
+            acts.append(("land",))
+        for w in (0, 1):
+            if finished[w]:
+                continue
+            if lookahead and pos[w] > 0:
+                # releases due after the previous tile: loads before the next tile's request
+                upto = tile_req[tiles[w][pos[w]]] if pos[w] < len(tiles[w]) else tile_req[tiles[w][pos[w] - 1]] + 1
+                if done[w] < upto:
+                    if done[w] < waited[w]:
+                        acts.append(("release", w))
+                    else:
+                        j = waited[w]
+                        if (full_ph[j & 1] & 1) != ((j >> 1) & 1):
+                            acts.append(("wait", w))
+                    continue
+            if pos[w] < len(tiles[w]):
+                if not landed(tiles[w][pos[w]]):
+                    continue
+                qi = tile_req[tiles[w][pos[w]]]
+                if done[w] < qi and done[w] < waited[w]:
+                    acts.append(("release", w))
+                elif waited[w] <= qi:
+                    j = waited[w]
+                    if (full_ph[j & 1] & 1) != ((j >> 1) & 1):   # the parity wait passes (early or not)
+                        acts.append(("wait", w))
+                else:
+                    acts.append(("tile", w))
+            else:
+                acts.append(("finish", w))
+        if not acts:
+            return "ok" if issued == n_req and all(finished.values()) else "deadlock"
+        a = rnd.choice(acts)
+        if a[0] == "issue":
+            j = issued
+            if j >= 2:
+                if empty_ph[j & 1] <= (j - 2) >> 1:
+                    return "early"
+                # the warps' tiles of request j - 2 must all be done
+                for w in (0, 1):
+                    if pos[w] < len(tiles[w]) and tile_req[tiles[w][pos[w]]] <= j - 2:
+                        return "overwrite"
+            issued += 1
+            in_flight.append(j)
+        elif a[0] == "walk":
+            walked += 1
+        elif a[0] == "land":
+            j = in_flight.pop(0)                  # TMA loads of one slot land in order
+            full_ph[j & 1] += 1
+        elif a[0] == "wait":
+            w = a[1]
+            j = waited[w]
+            if j >= issued or full_ph[j & 1] <= j >> 1:
+                return "early"
+            waited[w] += 1
+        elif a[0] == "release":
+            w = a[1]
+            j = done[w]
+            empty_arr[j & 1].append(j)
+            if any(x != empty_ph[j & 1] * 2 + (j & 1) for x in empty_arr[j & 1]):
+                return "miscount"
+            if len(empty_arr[j & 1]) == 2:
+                empty_ph[j & 1] += 1
+                empty_arr[j & 1] = []
+            done[w] += 1
+        elif a[0] == "tile":
+            w = a[1]
+            pos[w] += 1
+        else:
+            w = a[1]
+            while done[w] < waited[w]:
+                j = done[w]
+                empty_arr[j & 1].append(j)
+                if any(x != empty_ph[j & 1] * 2 + (j & 1) for x in empty_arr[j & 1]):
+                    return "miscount"
+                if len(empty_arr[j & 1]) == 2:
+                    empty_ph[j & 1] += 1
+                    empty_arr[j & 1] = []
+                done[w] += 1
+            finished[w] = True
+
+
+def _random_tiles(rnd, n_req):
+    reqs = []
+    for r in range(n_req):
+        reqs += [r] * rnd.choice([1, 1, 2, 3, 5])
+    return reqs
+
+
+@pytest.mark.parametrize("n_req", [1, 2, 3, 7, 20])
+def test_two_mma_warps_q_slots_sound_and_live(n_req):
+    rnd = random.Random(n_req)
+    for case in range(40):
+        tiles = _random_tiles(rnd, n_req)
+        for seed in range(25):
+            assert simulate_q(tiles, seed * 1000 + case) == "ok", (tiles, seed)
+
+
+@pytest.mark.parametrize("n_req", [1, 2, 3, 7, 20])
+def test_two_mma_warps_releasing_by_lookahead_live_with_a_coupled_q_producer(n_req):
+    # The warp that loads Q also issues the even tiles (waiting for each Q
+    # slot's release in order); the MMA warps release a load as soon as their
+    # own tiles are past its request, known from their own walk of the tiles.
+    rnd = random.Random(100 + n_req)
+    for case in range(40):
+        tiles = _random_tiles(rnd, n_req)
+        for seed in range(25):
+            assert simulate_q(tiles, seed * 1000 + case, coupled=True, lookahead=True) == "ok", (tiles, seed)
+
+
+def test_q_loads_by_a_tile_producer_can_deadlock_with_two_mma_warps():
+    # Why the Q loads get a warp of their own: when the warp that loads Q also
+    # issues the even tiles, a Q load waiting for the release of load q - 2
+    # holds back the next even tile, and the MMA warp of the even tiles reads
+    # that tile's request before it releases load q - 2.  Here request 1 is
+    # one odd tile: load 2 waits for the even warp to pass request 0, which
+    # it does at tile 2, issued after load 2.
+    tiles = [0, 1, 2, 2, 3, 3]
+    outcomes = {simulate_q(tiles, seed, coupled=True) for seed in range(300)}
+    assert outcomes == {"deadlock"}, outcomes
+    outcomes = {simulate_q(tiles, seed) for seed in range(300)}
+    assert outcomes == {"ok"}, outcomes
+
+
+def test_releasing_after_waiting_for_the_current_load_deadlocks():
+    # A first form: a warp at a tile of request q waited for every load up
+    # to q, then released the loads before q.  Load q needs the release of
+    # load q - 2, which that warp gives only after waiting for load q.
+    tiles = [0, 0, 0, 0, 0, 1, 2, 3]
+    assert simulate_q_wait_then_release(tiles) == "deadlock"
+
+
+def simulate_q_wait_then_release(tile_req):
+    """Deterministic schedule of the first form: warp 1 (odd tiles) runs
+    ahead; the producer issues whenever it can; loads land at once."""
+    n_req = tile_req[-1] + 1
+    empty_arr = [0] * n_req
+    issued = 0
+    tiles = {w: [tile_req[i] for i in range(len(tile_req)) if i % 2 == w] for w in (0, 1)}
+    pos = {0: 0, 1: 0}
+    waited = {0: 0, 1: 0}
+    progress = True
+    while progress:
+        progress = False
+        while issued < n_req and (issued < 2 or empty_arr[issued - 2] == 2):
+            issued += 1
+            progress = True
+        for w in (1, 0):
+            if pos[w] < len(tiles[w]):
+                qi = tiles[w][pos[w]]
+                if qi < issued:                    # waits for loads up to qi, all landed
+                    for j in range(waited[w], qi):
+                        empty_arr[j] += 1
+                    waited[w] = max(waited[w], qi)
+                    pos[w] += 1
+                    progress = True
+    return "ok" if all(pos[w] == len(tiles[w]) for w in (0, 1)) else "deadlock"
+
+
+def test_releasing_only_at_a_requests_last_tile_deadlocks_with_two_warps():
+    # Why every warp releases every load: with the single warp's rule (release
+    # at the request's last tile, here by the warp that has it), a barrier of
+    # count 2 never completes for a request one warp never touches.
+    def simulate_last_tile_rule(tile_req):
+        n_req = tile_req[-1] + 1
+        arrivals = [0] * n_req
+        for i, r in enumerate(tile_req):
+            if i == len(tile_req) - 1 or tile_req[i + 1] != r:
+                arrivals[r] += 1
+        # the producer needs the release of load j - 2 (two arrivals) to issue load j
+        return all(arrivals[j - 2] >= 2 for j in range(2, n_req))
+    assert not simulate_last_tile_rule([0, 1, 2, 3, 3])
