@@ -63,6 +63,7 @@ struct LogitsArgs {
 
 cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream);
 cudaError_t launch_logits_tc_interleaved(const LogitsArgs& a, cudaStream_t stream);
+cudaError_t launch_logits_tc_dual(const LogitsArgs& a, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int mode, long long cycles, uint32_t* status, cudaStream_t stream);
 
 struct TopKArgs {

@@ -129,7 +129,7 @@ constexpr int deepest_sound_ring(int fit, int producers, int jobs_per_tile) {
 // IL: K pages in the interleaved layout (each token's 128 value bytes then its
 // 4 scale bytes), copied into the stage as stored and rewritten there into the
 // MMA layout by the producers.
-template <int NEXT_N, int H, bool IL = false>
+template <int NEXT_N, int H, bool IL = false, bool DUAL_OK = false>
 struct Cfg {
   static constexpr int N = NEXT_N * H;
   static constexpr int NC = N <= 256 ? N : (N % 256 == 0 ? 256 : H);   // accumulator columns per job
@@ -157,8 +157,11 @@ struct Cfg {
   // warp's per-tile loop, not the tensor pipe, sets the tile rate): two MMA
   // warps take alternate tiles (warp kMmaWarp the even ones, warp 2 the odd
   // ones), each with its own two of the four accumulators, fed by two
-  // producer warps.  An even ring gives every stage to one MMA warp.
-  static constexpr bool DUAL = !IL && C == 1 && N <= 128;
+  // producer warps.  An even ring gives every stage to one MMA warp.  Only
+  // where the launch asks for it (DUAL_OK: pages of 64 tokens or more, at
+  // most two per tile): a tile of small pages costs its producer a copy-
+  // engine operation per page and scale run, and two producers fall behind.
+  static constexpr bool DUAL = DUAL_OK && !IL && C == 1 && N <= 128;
   static constexpr int PRODUCERS = DUAL ? 2 : (ring_waits_unambiguous(FIT, kProducers, C) ? kProducers : 2);
   static constexpr int STAGES = deepest_sound_ring(FIT, PRODUCERS, C);
   static_assert(STAGES >= 2 && ring_waits_unambiguous(STAGES, PRODUCERS, C), "shared memory");
@@ -674,11 +677,11 @@ struct Filler {
   }
 };
 
-template <int NEXT_N, int H, bool FUSED, bool IL>
+template <int NEXT_N, int H, bool FUSED, bool IL, bool DUAL_OK>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
                  const TcParams p) {
-  using K = Cfg<NEXT_N, H, IL>;
+  using K = Cfg<NEXT_N, H, IL, DUAL_OK>;
   constexpr int NP = K::PRODUCERS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1315,9 +1318,9 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-template <int NEXT_N, int H, bool FUSED, bool IL>
+template <int NEXT_N, int H, bool FUSED, bool IL, bool DUAL_OK = false>
 cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
-  using K = Cfg<NEXT_N, H, IL>;
+  using K = Cfg<NEXT_N, H, IL, DUAL_OK>;
   EncodeTiled enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const int P = a.page_size;
@@ -1358,7 +1361,7 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   static int smem_set[64] = {0};
   static_assert(!FUSED || K::STAGES * kStageBytes + 2 * K::Q_BYTES >= (int)kSelectSmem + 1024 + 4 * 8192,
                 "fused top-k scratch (and the keys of 8192-column rows) fit the drained K stages and Q slots");
-  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED, IL>, smem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(logits_tc_kernel<NEXT_N, H, FUSED, IL, DUAL_OK>, smem, smem_set);
   if (e != cudaSuccess) return e;
 
   TcParams p;
@@ -1382,17 +1385,31 @@ cudaError_t launch_tc(const LogitsArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H, FUSED, IL>, tkv, tq, p);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, logits_tc_kernel<NEXT_N, H, FUSED, IL, DUAL_OK>, tkv, tq, p);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-#ifndef SAI_LOGITS_INTERLEAVED
-cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream) {
+#if defined(SAI_LOGITS_DUAL)
+// Page-split caches with pages of 64 tokens or more, on the shapes whose
+// tiles are one job of at most 128 columns: two MMA warps (Cfg::DUAL).
+cudaError_t launch_logits_tc_dual(const LogitsArgs& a, cudaStream_t stream) {
   const bool fused = a.indices != nullptr;
   switch (a.next_n * 1000 + a.heads) {
+    case 1064: return fused ? launch_tc<1, 64, true, false, true>(a, stream) : launch_tc<1, 64, false, false, true>(a, stream);
+    case 2064: return fused ? launch_tc<2, 64, true, false, true>(a, stream) : launch_tc<2, 64, false, false, true>(a, stream);
+    case 1128: return fused ? launch_tc<1, 128, true, false, true>(a, stream) : launch_tc<1, 128, false, false, true>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+#elif !defined(SAI_LOGITS_INTERLEAVED)
+cudaError_t launch_logits_tc(const LogitsArgs& a, cudaStream_t stream) {
+  const bool fused = a.indices != nullptr;
+  const int shape = a.next_n * 1000 + a.heads;
+  if (a.page_size >= 64 && (shape == 1064 || shape == 2064 || shape == 1128)) return launch_logits_tc_dual(a, stream);
+  switch (shape) {
     case 1064: return fused ? launch_tc<1, 64, true, false>(a, stream) : launch_tc<1, 64, false, false>(a, stream);
     case 2064: return fused ? launch_tc<2, 64, true, false>(a, stream) : launch_tc<2, 64, false, false>(a, stream);
     case 3064: return fused ? launch_tc<3, 64, true, false>(a, stream) : launch_tc<3, 64, false, false>(a, stream);
