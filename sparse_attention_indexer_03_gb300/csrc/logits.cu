@@ -422,20 +422,23 @@ struct ScalarCursor {
 // Each CTA adds, per request it touched, the number of that request's tiles it
 // processed to the request's counter once its logits are stored and fenced;
 // the CTA whose addition completes the request's tile count resets the
-// counter to 0 and pushes the request's rows onto a queue of ready rows.
-// Every CTA, once its tiles are done, takes rows from the queue (one atomic
-// on its head per row) and selects them, reading the logits through L2; so
-// the selection is spread over the whole grid and starts as soon as a
-// request is complete.  A queue entry not yet written (its request still has
-// tiles in flight on another CTA) is waited for, with a bounded wait; the
-// grid is one CTA per SM, so every CTA is resident.  The last CTA to finish
-// resets the queue's head and tail; the workspace is all zero again.
-// Requests without tiles get their -1 rows from CTA (b mod grid).  Where
-// the -inf fill outweighs the tiles (more than four fill units per tile) the
-// two epilogue warpgroups select (NT = 256) while the other warps keep
-// writing the fill; elsewhere all warps select (NT = 384).  Named barrier 1
-// joins the selecting threads; the drained K-stage ring and Q slots hold the
-// selection's histograms and staged keys.
+// counter to 0 and publishes the request: its rows longer than k go onto a
+// queue of ready rows, its shorter ones (indices 0 .. n - 1, then -1) it
+// writes itself.  Every CTA, once its tiles are done, takes rows from the
+// queue (one atomic on its head per row, the next taken before the current
+// row is selected) and selects them, reading the logits through L2; so the
+// selection is spread over the whole grid and starts as soon as a request is
+// complete.  The queue's length (the launch's rows longer than k) comes from
+// the partition.  A queue entry not yet written (its request still has tiles
+// in flight on another CTA) is waited for, with a bounded wait; the grid is
+// one CTA per SM, so every CTA is resident.  The last CTA to finish resets
+// the queue's head, tail and done count and the fill counter; the workspace
+// is all zero again.  Requests without tiles get their -1 rows from CTA
+// (b mod grid).  Where the -inf fill outweighs the tiles (more than four
+// fill units per tile) the two epilogue warpgroups select (NT = 256) while
+// the other warps keep writing the fill; elsewhere all warps select
+// (NT = 384).  Named barrier 1 joins the selecting threads; the drained
+// K-stage ring and Q slots hold the selection's histograms and staged keys.
 template <int NT>
 struct TailBar {
   __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
