@@ -30,7 +30,10 @@
 //   warp 3     TMEM allocation and the MMA issuer: tcgen05.mma kind::f8f6f4,
 //              A = the K stage (128 tokens x 128 B, K-major, 128-byte
 //              swizzle), B = Q (whole rows j, <= 256 columns per job), fp32
-//              accumulators in a ring of TMEM stages.
+//              accumulators in a ring of TMEM stages.  On decode-like shapes
+//              (one job of <= 128 columns per tile) with pages of >= 64
+//              tokens, warp 2 is a second MMA issuer taking the odd tiles
+//              (Cfg::DUAL; compiled in logits_dual.cu) and warps 0-1 produce.
 //   warps 4-11 two epilogue warpgroups taking alternate jobs: tcgen05.ld of a
 //              token's accumulator row, ReLU, per-head weight, scale, -inf
 //              mask, coalesced stores at a 64-bit row base (aiter PR 4244,
@@ -40,7 +43,9 @@
 // Work partition: the 128-token tiles of all requests, in request order,
 // split into equal contiguous ranges, one per CTA; the fill split the same
 // way in units of (row, 4096 columns).  Each CTA derives its range from
-// context_lens itself; there is no global scratch and no atomics.
+// context_lens itself, with no global scratch and no atomics.  (The fused
+// launch adds per-request counters and a ready-row queue in its workspace,
+// and shares a fill-heavy launch's fill units through one counter there.)
 //
 // Every wait is bounded: when one runs out, the CTA raises SAI_STATUS_TIMEOUT,
 // stops, lets its in-flight copies and MMAs drain (again bounded), frees its
