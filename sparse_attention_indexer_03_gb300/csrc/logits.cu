@@ -249,21 +249,31 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
   static_assert(32 * kCtxRegs == kCtxSmem, "every request of a staged batch is read by the register path");
   if (p.batch <= 32 * kCtxRegs) {
     const int R = (p.batch + 31) / 32;
-    int32_t tl[kCtxRegs], ul[kCtxRegs];
-    int64_t lt = 0, lu = 0;
+    // Every load of the lane's lengths is in flight before the first use;
+    // the per-request sums then cover the lane's R requests only.
+    int32_t rl[kCtxRegs], tl[kCtxRegs], ul[kCtxRegs];
 #pragma unroll
     for (int x = 0; x < kCtxRegs; ++x) {
       const int b = lane * R + x;
-      const bool v = x < R && b < p.batch;
-      const int64_t raw = v ? (int64_t)p.context_lens[b] : 0;
-      if (v) ctx_s[b] = (int32_t)raw;
-      clamped |= v && (raw < 0 || raw > p.cap);
+      rl[x] = x < R && b < p.batch ? p.context_lens[b] : 0;
+      tl[x] = 0;
+      ul[x] = 0;
+    }
+    int64_t lt = 0, lu = 0;
+#pragma unroll
+    for (int x = 0; x < kCtxRegs; ++x) {
+      if (x >= R) break;
+      const int b = lane * R + x;
+      if (b >= p.batch) continue;
+      const int64_t raw = rl[x];
+      ctx_s[b] = rl[x];
+      clamped |= raw < 0 || raw > p.cap;
       const int64_t ce = ctx_eff(raw, p.cap);
       tl[x] = (int32_t)req_tiles(ce);
-      ul[x] = v ? (int32_t)req_units<NEXT_N>(ce, p.width) : 0;
+      ul[x] = (int32_t)req_units<NEXT_N>(ce, p.width);
       lt += tl[x];
       lu += ul[x];
-      if (v && p.k > 0)
+      if (p.k > 0)
         for (int j = 0; j < NEXT_N; ++j) with_tiles += row_context(raw, NEXT_N, j, p.cap) > p.k ? 1 : 0;
     }
     const int64_t it = warp_incl_scan64(lt, lane), iu = warp_incl_scan64(lu, lane);
@@ -275,6 +285,7 @@ __device__ void compute_partition(const TcParams& p, Part* part, int32_t* ctx_s,
     int64_t at = it - lt, au = iu - lu;              // units before this lane's first request
 #pragma unroll
     for (int x = 0; x < kCtxRegs; ++x) {
+      if (x >= R) break;
       if (tl[x] > 0 && at <= tb && tb < at + tl[x]) { fb = lane * R + x; ft = (int)(tb - at); }
       if (ul[x] > 0 && au <= ub && ub < au + ul[x]) { gb = lane * R + x; gu = (int)(ub - au); }
       at += tl[x];
