@@ -130,22 +130,34 @@ def describe(w) -> str:
             f"W={w.max_model_len}, stride={w.logits_stride}, k={w.topk}, seed={w.seed}")
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+# The logits kernel's source: its file and the headers it includes (the
+# fused launch's row selection lives in select.cuh).
+LOGITS_SOURCES = ("logits.cu", "select.cuh", "ptx.cuh", "common.cuh")
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def logits_source_sha() -> str:
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_03_gb300", "csrc")
+    return source_sha([os.path.join(csrc, f) for f in LOGITS_SOURCES])
 
 
 def profiled_traffic(workload: str, fused: bool = False):
     """DRAM bytes per logits launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    taken on the current kernel source (logits_source_sha); else None."""
     path = os.path.join(ROOT, "profiles", f"logits_tc{'_topk' if fused else ''}_{workload}.md")
-    src = os.path.join(ROOT, "sparse_attention_indexer_03_gb300", "csrc", "logits.cu")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_sha(src):
+    if not m or not s or s.group(1) != logits_source_sha():
         return None
     return int(m.group(1))
 

@@ -127,8 +127,9 @@ __device__ __forceinline__ SelectResult radix_select(SelectShared<NT>& sh, uint3
     const uint32_t wsum = __reduce_add_sync(0xffffffffu, mine);
     if (lane == 0) sh.wtot[warp] = wsum;
     bar();
-    uint32_t above = 0;                             // keys in the warps above this one
-    for (int w = warp + 1; w < kW; ++w) above += sh.wtot[w];
+    // Keys in the warps above this one: lane l reads warp l's total, one
+    // warp reduction sums them (no chain of dependent shared reads).
+    uint32_t above = __reduce_add_sync(0xffffffffu, lane > warp && lane < kW ? sh.wtot[lane] : 0u);
     const uint32_t rem = s.remaining;
     if (above < rem && above + wsum >= rem) {       // warp-uniform: the bin is in this warp
 #pragma unroll
@@ -191,8 +192,8 @@ __device__ __forceinline__ void compact_stream(SelectShared<NT>& sh, const Selec
   c_eq = __reduce_add_sync(0xffffffffu, c_eq);
   if (lane == 0) { sh.warp_gt[warp] = c_gt; sh.warp_eq[warp] = c_eq; }
   bar();
-  uint32_t off_gt = 0, off_eq = 0;
-  for (int w = 0; w < warp; ++w) { off_gt += sh.warp_gt[w]; off_eq += sh.warp_eq[w]; }
+  uint32_t off_gt = __reduce_add_sync(0xffffffffu, lane < warp ? sh.warp_gt[lane] : 0u);   // the warps before
+  uint32_t off_eq = __reduce_add_sync(0xffffffffu, lane < warp ? sh.warp_eq[lane] : 0u);
   const uint32_t lt = (1u << lane) - 1u;
   for (int64_t base = lo; base < hi; base += 32 * kU) {
     uint32_t m[kU];
@@ -255,8 +256,9 @@ __device__ __forceinline__ void compact_lanes(SelectShared<NT>& sh, const Select
   if (lane == 31) { sh.warp_gt[warp] = incl >> 16; sh.warp_eq[warp] = incl & 0xffffu; }
   bar();
   const uint32_t excl = incl - x;
-  uint32_t pg = excl >> 16, pe = excl & 0xffffu;
-  for (int w = 0; w < warp; ++w) { pg += sh.warp_gt[w]; pe += sh.warp_eq[w]; }
+  // Plus the counts of the warps before this one (lane l reads warp l's).
+  uint32_t pg = (excl >> 16) + __reduce_add_sync(0xffffffffu, lane < warp ? sh.warp_gt[lane] : 0u);
+  uint32_t pe = (excl & 0xffffu) + __reduce_add_sync(0xffffffffu, lane < warp ? sh.warp_eq[lane] : 0u);
   preceding(sh, pg, pe);
   key_at.for_each([&](int i, uint32_t key) {
     const uint32_t m = key & s.mask;
