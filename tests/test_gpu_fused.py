@@ -135,6 +135,21 @@ def test_fill_heavy_launch(next_n, heads):
     _check(w, k=2048)
 
 
+@pytest.mark.parametrize("batch", [1, 31, 32, 33, 95, 511, 512, 513])
+def test_partition_batch_edges(batch):
+    # The work partition reads a batch of up to 512 requests R = ceil(B / 32)
+    # per lane (the last lanes partly or wholly past the batch) and walks
+    # larger batches 32 requests at a time: batch sizes at those edges, with
+    # empty requests and requests of one tile, through both launches.
+    rng = np.random.default_rng(batch)
+    ctx = rng.integers(0, 600, size=batch)
+    ctx[::7] = 0
+    ctx[1::11] = 128
+    w = synth.custom(batch=batch, next_n=2, heads=64, page_size=16, context_lens=ctx, max_model_len=640,
+                     seed=500 + batch)
+    _check(w, k=64)
+
+
 def test_all_contexts_empty():
     w = synth.custom(batch=5, next_n=2, heads=64, page_size=16, context_lens=[0, 0, 0, 0, 0],
                      max_model_len=256, seed=3)
