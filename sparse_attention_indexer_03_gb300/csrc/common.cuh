@@ -76,6 +76,7 @@ struct TopKArgs {
   int k;
   int32_t* indices;
   int64_t out_stride;
+  bool longest_first = false;   // set by launch_topk: CTAs take the rows longest first
 };
 
 cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream);

@@ -214,15 +214,85 @@ topk_cluster_kernel(TopKArgs a) {
 // columns than their width) go to CTAs of 512 threads staging up to 16384
 // keys (112 KB), two per SM: the select's phases are latency-bound, so two
 // rows in flight overlap them.
+// ---- longest rows first: when the grid is several waves, position p takes the
+// row of rank p in an order by request length class (floor(log2) of the
+// context, longest class first, request order within a class; a request's
+// rows stay together), so the longest rows start in the first wave and the
+// last waves hold short ones.  Every CTA derives its row from the context
+// lengths: one coalesced read of all of them (the latency of its own row's
+// length read, which it replaces), a 32-bin histogram, a warp scan, and one
+// block-wide count of the chosen class.  Batches of at most NT requests.
+template <int NT>
+struct LongestFirst {
+  uint32_t bins[32];
+  uint32_t wcnt[NT / 32];
+  int cls, off, b, ctx;
+};
+
+__device__ __forceinline__ int length_class(int64_t ctx, int64_t width) {
+  const int64_t ce = ctx < 0 ? 0 : (ctx > width ? width : ctx);
+  const uint32_t c = (uint32_t)(ce > 0x7fffffff ? 0x7fffffff : ce);
+  return c <= 1 ? 31 : __clz(c);                         // 31 - floor(log2 c): the longest first
+}
+
+// Row of grid position p; *ctx its request's context length.
+template <int NT>
+__device__ __forceinline__ int64_t longest_first_row(const TopKArgs& a, int64_t p, LongestFirst<NT>& lf,
+                                                     int64_t* ctx) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t q = p / a.next_n;                        // the request's rank
+  const bool have = tid < a.batch;
+  const int32_t c_me = have ? a.context_lens[tid] : 0;
+  const int key = have ? length_class(c_me, a.width) : -1;
+  if (tid < 32) lf.bins[tid] = 0u;
+  __syncthreads();
+  if (have) atomicAdd(&lf.bins[key], 1u);
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t cnt = lf.bins[lane];
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t excl = incl - cnt;
+    if (excl <= (uint64_t)q && (uint64_t)q < incl) {     // one lane: q < batch
+      lf.cls = lane;
+      lf.off = (int)(q - excl);
+    }
+  }
+  __syncthreads();
+  const bool mine = key == lf.cls;
+  const uint32_t bal = __ballot_sync(0xffffffffu, mine);
+  if (lane == 0) lf.wcnt[warp] = __popc(bal);
+  __syncthreads();
+  const uint32_t before = __reduce_add_sync(0xffffffffu, lane < warp ? lf.wcnt[lane] : 0u);
+  if (mine && before + __popc(bal & ((1u << lane) - 1u)) == (uint32_t)lf.off) {
+    lf.b = tid;
+    lf.ctx = c_me;
+  }
+  __syncthreads();
+  *ctx = lf.ctx;
+  return (int64_t)lf.b * a.next_n + p % a.next_n;
+}
+
 template <int NT, int KEYS>
 __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1)
 topk_smem_kernel(TopKArgs a) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
   __shared__ SelectShared<NT> sh;
+  __shared__ LongestFirst<NT> lf;
   ptx::wait_prerequisites();
   ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
-  const int64_t r = blockIdx.x;
-  const int64_t n = row_len(a, r);
+  int64_t r = blockIdx.x, n;
+  if (a.longest_first) {
+    int64_t ctx;
+    r = longest_first_row<NT>(a, blockIdx.x, lf, &ctx);
+    n = row_context(ctx, a.next_n, (int)(r % a.next_n), a.width);
+  } else {
+    n = row_len(a, r);
+  }
   int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
   if (n <= a.k) {
     for (int i = threadIdx.x; i < a.k; i += NT) out[i] = i < n ? i : -1;
@@ -281,6 +351,13 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   // single 131072-column row: 37 us against 30 us.)
   const int sms = device_sm_count();
   const int64_t slices = (a.width + kClusterSlice - 1) / kClusterSlice;
+  // More rows than one wave of the one-row-per-CTA kernels below: take them
+  // longest first (for batches of at most one CTA's threads).
+  auto lpt = [&](int ctas_per_sm, int nt) {
+    TopKArgs b = a;
+    b.longest_first = rows > (int64_t)ctas_per_sm * (sms > 0 ? sms : 152) && a.batch <= nt;
+    return b;
+  };
   const int cl = slices <= 2 ? 2 : (slices <= 4 ? 4 : 8);
   const bool clustered = a.width > kClusterSlice && slices <= 8 && rows * cl <= 4 * (int64_t)(sms > 0 ? sms : 152);
   cudaError_t e;
@@ -293,11 +370,11 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   else if (a.width <= 8 * kThreads) e = launch_pdl(topk_reg_kernel<8>, g, a, stream, set8, kSelectSmem, kSelectSmem);
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
   else if (a.width <= kSmemKeysWide)
-    e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, a, stream, set_smem,
+    e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, lpt(1, kThreads), stream, set_smem,
                    kSelectSmem + 4 * (size_t)(a.width + 4), smem_keys_bytes<kSmemKeysWide>());
   else
-    e = launch_pdl(topk_smem_kernel<512, kSmemKeysPair>, g, a, stream, set_pair, smem_keys_bytes<kSmemKeysPair>(),
-                   smem_keys_bytes<kSmemKeysPair>(), 1, 512);
+    e = launch_pdl(topk_smem_kernel<512, kSmemKeysPair>, g, lpt(2, 512), stream, set_pair,
+                   smem_keys_bytes<kSmemKeysPair>(), smem_keys_bytes<kSmemKeysPair>(), 1, 512);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
