@@ -277,6 +277,29 @@ __device__ __forceinline__ int64_t longest_first_row(const TopKArgs& a, int64_t 
   return (int64_t)lf.b * a.next_n + p % a.next_n;
 }
 
+// One row r of n columns by a CTA of NT threads: the histograms at the start
+// of `topk_smem`, up to KEYS staged keys after them (longer rows, where
+// STREAM, re-read from L2 per pass).  Ends with every thread done with the
+// shared memory (a barrier), except for a row of at most k columns, which
+// uses none.
+template <int NT, int KEYS, bool STREAM = true>
+__device__ __forceinline__ void smem_row(const TopKArgs& a, int64_t r, int64_t n, uint8_t* topk_smem,
+                                         SelectShared<NT>& sh) {
+  int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
+  if (n <= a.k) {
+    for (int i = threadIdx.x; i < a.k; i += NT) out[i] = i < n ? i : -1;
+    return;
+  }
+  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem);
+  const float* row = a.logits + r * a.stride;
+  if (!STREAM || n <= KEYS) {
+    uint32_t* key_base = reinterpret_cast<uint32_t*>(topk_smem + kSelectSmem);
+    topk_row_staged<NT>(row, (int)n, a.k, out, sh, hist, key_base, threadIdx.x, CtaBar{});
+  } else {
+    topk_row_stream<NT>(row, n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
+  }
+}
+
 template <int NT, int KEYS>
 __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1)
 topk_smem_kernel(TopKArgs a) {
@@ -293,18 +316,78 @@ topk_smem_kernel(TopKArgs a) {
   } else {
     n = row_len(a, r);
   }
-  int32_t* out = a.indices + r * a.out_stride;             // 64-bit row base
-  if (n <= a.k) {
-    for (int i = threadIdx.x; i < a.k; i += NT) out[i] = i < n ? i : -1;
-    return;
+  smem_row<NT, KEYS>(a, r, n, topk_smem, sh);
+}
+
+// ---- many rows of up to KEYS staged keys, longest first, on one CTA per SM
+// that keeps its shared memory across rows: the CTA ranks the batch's
+// requests once (as above, into a permutation kept after the key staging
+// area: a request's rank is the start of its class plus the requests of its
+// class in earlier warps and in earlier lanes of its warp), then takes the
+// grid positions b, 2G - 1 - b, 2G + b, ... (alternating direction per wave
+// of G positions, so each CTA takes one row of every length tier).  Saves the
+// per-row ranking and CTA start of the one-row-per-CTA form, which most rows
+// of a batch of short requests pay for a row of at most k columns.
+template <int NT>
+struct RowOrder {
+  uint16_t perm[NT];              // request of each rank
+  int32_t ctx[NT];                // each request's context length
+};
+
+template <int KEYS>
+constexpr size_t row_order_offset(int64_t width) { return (kSelectSmem + 4 * ((size_t)width + 4) + 15) / 16 * 16; }
+
+template <int KEYS>
+__global__ void __launch_bounds__(kThreads, 1)
+topk_smem_ordered_kernel(TopKArgs a) {
+  constexpr int NT = kThreads, kW = NT / 32;
+  extern __shared__ __align__(16) uint8_t topk_smem[];
+  __shared__ SelectShared<NT> sh;
+  ptx::wait_prerequisites();
+  ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
+  RowOrder<NT>& ro = *reinterpret_cast<RowOrder<NT>*>(topk_smem + row_order_offset<KEYS>(a.width));
+  {
+    // Ranking scratch in the key staging area (no row staged yet).
+    uint32_t(*wc)[32] = reinterpret_cast<uint32_t(*)[32]>(topk_smem + kSelectSmem);   // [warp][class]
+    uint32_t* cpre = wc[kW];                                                             // [class]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool have = tid < a.batch;
+    const int32_t c_me = have ? a.context_lens[tid] : 0;
+    const int key = have ? length_class(c_me, a.width) : -1;
+    if (have) ro.ctx[tid] = c_me;
+    wc[warp][lane] = 0u;
+    __syncwarp();
+    const uint32_t same = __match_any_sync(0xffffffffu, key);
+    const uint32_t lower = __popc(same & ((1u << lane) - 1u));   // equal keys in earlier lanes
+    if (have && lower == 0) wc[warp][key] = __popc(same);
+    __syncthreads();
+    if (warp == 0) {                             // lane c: class c's prefix over warps, then over classes
+      uint32_t run = 0;
+      for (int w = 0; w < kW; ++w) {
+        const uint32_t v = wc[w][lane];
+        wc[w][lane] = run;
+        run += v;
+      }
+      uint32_t incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      cpre[lane] = incl - run;
+    }
+    __syncthreads();
+    if (have) ro.perm[cpre[key] + wc[warp][key] + lower] = (uint16_t)tid;
+    __syncthreads();                             // the permutation is complete; the scratch is free
   }
-  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem);
-  const float* row = a.logits + r * a.stride;
-  if (n <= KEYS) {
-    uint32_t* key_base = reinterpret_cast<uint32_t*>(topk_smem + kSelectSmem);
-    topk_row_staged<NT>(row, (int)n, a.k, out, sh, hist, key_base, threadIdx.x, CtaBar{});
-  } else {
-    topk_row_stream<NT>(row, n, a.k, out, sh, hist, threadIdx.x, CtaBar{});
+  const int rows = a.batch * a.next_n, G = (int)gridDim.x;      // batch <= NT
+  for (int t0 = 0, wave = 0; t0 < rows; t0 += G, ++wave) {
+    const int p = t0 + ((wave & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    if (p >= rows) continue;
+    const int b = ro.perm[p / a.next_n], j = p % a.next_n;
+    // (width <= KEYS: every row is staged)
+    smem_row<NT, KEYS, false>(a, (int64_t)b * a.next_n + j, row_context(ro.ctx[b], a.next_n, j, a.width),
+                              topk_smem, sh);
   }
 }
 
@@ -344,7 +427,7 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.batch * a.next_n;
   if (rows == 0) return cudaSuccess;
   const unsigned g = (unsigned)rows;
-  static int set4[64], set8[64], set16[64], set_smem[64], set_pair[64], set_c2[64], set_c4[64], set_c8[64];
+  static int set4[64], set8[64], set16[64], set_smem[64], set_ord[64], set_pair[64], set_c2[64], set_c4[64], set_c8[64];
   // Rows wider than one CTA's registers go to a cluster (16384 columns per
   // CTA) while the grid stays within four CTAs per SM; more rows fill the
   // GPU one CTA each.  (Clusters of 16 CTAs of 8192 columns were slower on a
@@ -369,8 +452,12 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   } else if (a.width <= 4 * kThreads) e = launch_pdl(topk_reg_kernel<4>, g, a, stream, set4, kSelectSmem, kSelectSmem);
   else if (a.width <= 8 * kThreads) e = launch_pdl(topk_reg_kernel<8>, g, a, stream, set8, kSelectSmem, kSelectSmem);
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
+  else if (a.width <= kSmemKeysWide && lpt(1, kThreads).longest_first)
+    e = launch_pdl(topk_smem_ordered_kernel<kSmemKeysWide>, (unsigned)(sms > 0 ? sms : 152), a, stream, set_ord,
+                   row_order_offset<kSmemKeysWide>(a.width) + sizeof(RowOrder<kThreads>),
+                   row_order_offset<kSmemKeysWide>(kSmemKeysWide) + sizeof(RowOrder<kThreads>));
   else if (a.width <= kSmemKeysWide)
-    e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, lpt(1, kThreads), stream, set_smem,
+    e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, a, stream, set_smem,
                    kSelectSmem + 4 * (size_t)(a.width + 4), smem_keys_bytes<kSmemKeysWide>());
   else
     e = launch_pdl(topk_smem_kernel<512, kSmemKeysPair>, g, lpt(2, 512), stream, set_pair,
