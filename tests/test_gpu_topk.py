@@ -100,13 +100,19 @@ def test_long_rows(W):
     assert_topk_exact(got, vals, n_r, k)
 
 
-@pytest.mark.parametrize("batch,next_n,W", [(300, 3, 32768), (1100, 1, 20000), (400, 2, 100000)])
+@pytest.mark.parametrize("batch,next_n,W", [(300, 3, 32768), (1100, 1, 20000), (400, 2, 100000),
+                                            (153, 1, 20000), (1024, 1, 20000), (1025, 1, 20000),
+                                            (77, 4, 40960)])
 def test_many_rows_longest_first(batch, next_n, W):
     # More rows than one wave of CTAs, on both shared-memory kernels (one CTA
-    # of 1024 threads per SM up to 40960 columns, two of 512 beyond, where
-    # rows longer than 16384 columns are re-read from L2 on each pass): the
-    # same sets as the oracle's top-k on the same values, and 0..n-1 then -1
-    # for the short rows.  Contexts span empty to the full width and repeat.
+    # of 1024 threads per SM up to 40960 columns, ranking the batch once and
+    # taking one row of every length tier; two of 512 beyond, each ranking
+    # for its own row, where rows longer than 16384 columns are re-read from
+    # L2 on each pass): one row past a wave (one CTA takes two rows), the
+    # largest batch the ranking takes (1024 requests) and one more (one CTA
+    # per row in row order), a request's rows kept together (next_n = 4).
+    # The same sets as the oracle's top-k on the same values, and 0..n-1 then
+    # -1 for the short rows.  Contexts span empty to the full width and repeat.
     rng = np.random.default_rng(batch + W)
     k = 2048
     ctx = np.exp(rng.uniform(0, np.log(W), size=batch)).astype(np.int64)
