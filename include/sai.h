@@ -239,8 +239,8 @@ SAI_API int sai_paged_mqa_logits_topk(const uint8_t* q_fp8, const uint8_t* kv_ca
  *     call that completes leaves it zero.  After a call that raised
  *     SAI_STATUS_TIMEOUT it may hold partial counts and queue entries, and
  *     later calls of this entry point on that device may select from
- *     incomplete rows: use sai_paged_mqa_logits_topk with a zeroed workspace
- *     from then on.
+ *     incomplete rows until sai_paged_mqa_logits_topk_static_reset has
+ *     zeroed it.
  *   - Concurrency: all calls on one device share the array.  Two calls in
  *     flight at once (on different streams, or from different threads
  *     without ordering) race on them and give wrong indices; order such calls
@@ -254,6 +254,18 @@ SAI_API int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t
                               float* logits, int64_t logits_stride, int64_t max_model_len,
                               int32_t k, int32_t* indices, int64_t indices_stride,
                               uint32_t* status, sai_stream_t stream);
+
+/*
+ * sai_paged_mqa_logits_topk_static_reset -- zero the static workspace of
+ * sai_paged_mqa_logits_topk_static on the current device (one memset of its
+ * 5 * 16384 + 4 int32 on `stream`; nothing is allocated).  After a call that
+ * raised SAI_STATUS_TIMEOUT, a reset ordered after that call and before the
+ * next one makes the static entry point usable again.  It races with a
+ * static call in flight on another stream, like two static calls do.
+ * Returns SAI_OK, or SAI_ERR_CUDA when the array's address cannot be looked
+ * up on the current device or the memset cannot be enqueued.
+ */
+SAI_API int sai_paged_mqa_logits_topk_static_reset(sai_stream_t stream);
 
 /*
  * sai_indexer_k_quant_insert -- quantise new K rows to FP8 and write them into

@@ -24,6 +24,7 @@ __all__ = [
     "LibraryNotBuilt", "SaiError", "build", "library", "library_path",
     "paged_mqa_logits", "top_k_workspace_bytes", "top_k_per_row_decode",
     "logits_topk_workspace_bytes", "paged_mqa_logits_topk", "paged_mqa_logits_topk_static",
+    "paged_mqa_logits_topk_static_reset",
     "indexer_k_quant_insert", "gather_selected_kv",
     "STATUS_BAD_PAGE", "STATUS_CTX_CLAMPED", "STATUS_TIMEOUT",
     "KV_PAGE_SPLIT", "KV_INTERLEAVED",
@@ -76,6 +77,7 @@ _SIGS = {
                                                     _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                                     _P, _c.c_int64, _c.c_int64, _c.c_int32, _P, _c.c_int64,
                                                     _P, _P]),
+    "sai_paged_mqa_logits_topk_static_reset": (_c.c_int, [_P]),
     "sai_indexer_k_quant_insert": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _P, _P, _c.c_int64, _c.c_int32,
                                               _c.c_int32, _P, _P]),
     "sai_gather_selected_kv": (_c.c_int, [_P, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _P, _c.c_int64,
@@ -240,6 +242,14 @@ def paged_mqa_logits_topk_static(q, kv_cache, page_size: int, weights, context_l
         _ptr(status, (torch.int32, torch.uint32), "status"), _stream_handle(stream))
     if code != OK:
         raise SaiError(code, "sai_paged_mqa_logits_topk_static")
+
+
+def paged_mqa_logits_topk_static_reset(stream=None) -> None:
+    """Zero the static workspace of `paged_mqa_logits_topk_static` on the
+    current device (after a call that raised STATUS_TIMEOUT)."""
+    code = library().sai_paged_mqa_logits_topk_static_reset(_stream_handle(stream))
+    if code != OK:
+        raise SaiError(code, "sai_paged_mqa_logits_topk_static_reset")
 
 
 def indexer_k_quant_insert(k, slot_mapping, kv_cache, page_size: int, *, num_pages: Optional[int] = None,

@@ -187,6 +187,15 @@ int sai_paged_mqa_logits_topk_static(const uint8_t* q_fp8, const uint8_t* kv_cac
   return from_cuda(launch_logits_tc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int sai_paged_mqa_logits_topk_static_reset(sai_stream_t stream) {
+  using namespace sai;
+  int32_t* counters = nullptr;
+  const int sc = static_counters(&counters);
+  if (sc != SAI_OK) return sc;
+  return from_cuda(cudaMemsetAsync(counters, 0, sizeof(int32_t) * fused_workspace_words(kStaticMaxBatch),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int sai_indexer_k_quant_insert(const uint16_t* k_bf16, int64_t num_tokens, int32_t head_dim,
                                const int64_t* slot_mapping, uint8_t* kv_cache, int64_t num_pages,
                                int32_t page_size, int32_t kv_layout, uint32_t* status, sai_stream_t stream) {

@@ -84,3 +84,31 @@ def test_two_calls_match_the_workspace_entry_point(name):
         fin = np.isfinite(ref)
         assert (np.abs(got[fin] - ref[fin]) <= ATOL + RTOL * np.abs(ref[fin])).all()
         assert torch.equal(idx, ref_idx)
+
+
+@pytest.mark.gpu
+def test_reset_between_calls_keeps_the_static_entry_point_exact():
+    # sai_paged_mqa_logits_topk_static_reset zeroes the static workspace on the
+    # caller's stream (the remedy after a call that raised STATUS_TIMEOUT):
+    # static calls before and after resets on the same stream still match the
+    # workspace entry point entry for entry.
+    import torch
+
+    sai.build()
+    lib = sai.library()
+    w = synth.decode()
+    dev = w.to_device()
+    k = w.topk
+    stream = torch.cuda.current_stream().cuda_stream
+    ref_logits = torch.empty((w.rows, w.logits_stride), dtype=torch.float32, device="cuda")
+    ref_idx = torch.full((w.rows, k), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sai.logits_topk_workspace_bytes(w.batch) // 4, dtype=torch.int32, device="cuda")
+    assert _call_workspace(lib, w, dev, ref_logits, ref_idx, k, ws, stream) == sai.OK
+    for _ in range(2):
+        sai.paged_mqa_logits_topk_static_reset()
+        logits = torch.full((w.rows, w.logits_stride), 99.0, dtype=torch.float32, device="cuda")
+        idx = torch.full((w.rows, k), -7, dtype=torch.int32, device="cuda")
+        assert _call_static(lib, w, dev, logits, idx, k, stream) == sai.OK
+        torch.cuda.synchronize()
+        assert torch.equal(idx, ref_idx)
+        assert torch.equal(logits[:, :w.max_model_len], ref_logits[:, :w.max_model_len])
