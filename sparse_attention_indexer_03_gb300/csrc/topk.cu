@@ -321,9 +321,10 @@ topk_smem_kernel(TopKArgs a) {
 
 // ---- many rows of up to KEYS staged keys, longest first, on one CTA per SM
 // that keeps its shared memory across rows: the CTA ranks the batch's
-// requests once (as above, into a permutation kept after the key staging
-// area: a request's rank is the start of its class plus the requests of its
-// class in earlier warps and in earlier lanes of its warp), then takes the
+// requests once in the order above (into a permutation kept after the key
+// staging area: a request's rank is the start of its class plus the requests
+// of its class in earlier warps and in earlier lanes of its warp, counted
+// per warp by one match instruction), then takes the
 // grid positions b, 2G - 1 - b, 2G + b, ... (alternating direction per wave
 // of G positions, so each CTA takes one row of every length tier).  Saves the
 // per-row ranking and CTA start of the one-row-per-CTA form, which most rows
@@ -334,7 +335,7 @@ struct RowOrder {
   int32_t ctx[NT];                // each request's context length
 };
 
-template <int KEYS>
+// The permutation's place: after the histograms and a row's staged keys.
 constexpr size_t row_order_offset(int64_t width) { return (kSelectSmem + 4 * ((size_t)width + 4) + 15) / 16 * 16; }
 
 template <int KEYS>
@@ -345,7 +346,7 @@ topk_smem_ordered_kernel(TopKArgs a) {
   __shared__ SelectShared<NT> sh;
   ptx::wait_prerequisites();
   ptx::launch_dependents();     // the next logits launch may take the SMs this grid leaves idle
-  RowOrder<NT>& ro = *reinterpret_cast<RowOrder<NT>*>(topk_smem + row_order_offset<KEYS>(a.width));
+  RowOrder<NT>& ro = *reinterpret_cast<RowOrder<NT>*>(topk_smem + row_order_offset(a.width));
   {
     // Ranking scratch in the key staging area (no row staged yet).
     uint32_t(*wc)[32] = reinterpret_cast<uint32_t(*)[32]>(topk_smem + kSelectSmem);   // [warp][class]
@@ -454,8 +455,8 @@ cudaError_t launch_topk(const TopKArgs& a, cudaStream_t stream) {
   else if (a.width <= 16 * kThreads) e = launch_pdl(topk_reg_kernel<16>, g, a, stream, set16, kSelectSmem, kSelectSmem);
   else if (a.width <= kSmemKeysWide && lpt(1, kThreads).longest_first)
     e = launch_pdl(topk_smem_ordered_kernel<kSmemKeysWide>, (unsigned)(sms > 0 ? sms : 152), a, stream, set_ord,
-                   row_order_offset<kSmemKeysWide>(a.width) + sizeof(RowOrder<kThreads>),
-                   row_order_offset<kSmemKeysWide>(kSmemKeysWide) + sizeof(RowOrder<kThreads>));
+                   row_order_offset(a.width) + sizeof(RowOrder<kThreads>),
+                   row_order_offset(kSmemKeysWide) + sizeof(RowOrder<kThreads>));
   else if (a.width <= kSmemKeysWide)
     e = launch_pdl(topk_smem_kernel<kThreads, kSmemKeysWide>, g, a, stream, set_smem,
                    kSelectSmem + 4 * (size_t)(a.width + 4), smem_keys_bytes<kSmemKeysWide>());
